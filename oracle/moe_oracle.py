@@ -1,0 +1,277 @@
+"""CPU oracle for the DeepSeekMoE layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+benchmark's CPU-baseline leg may import this module.  The product path (the
+CUDA library and its Python binding) never calls it and shares no code with it.
+
+Plain NumPy in float64, written straight from the equations on the source
+pages, with no blocking, fusion or reordering beyond what the equations state.
+Page titles cited below:
+
+  [FG]  "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE" (llm-infra-atlas): §2.1
+        segmentation and its Eq. 6–8 (softmax gating, top-mK, no
+        renormalisation); §2.2 the combination counts; §3.1 shared-expert
+        isolation Eq. 9–11 (h = Σ shared + Σ g·routed + u) and the DeepSeek-V3
+        form Eq. 12–15 (sigmoid scores, weights normalised over the selected).
+  [CH7] "MoE 的分水岭——DeepSeek 配方与 2026 年的主流形态" (ibossgateway,
+        ch. 7): §7.4, the per-expert bias b_i is added to the scores for the
+        choice only, the weights use the raw scores; §7.2 the counts C(8,2)
+        and "64 choose 8".
+  [PS]  "19-deepseek-moe" (ai.tomabc.com paper story): the expert FFN written
+        as ReLU(x W_i) then a projection (we drop the biases), and the
+        three-term forward (shared, routed, residual).
+
+Readings where the pages are silent or disagree (each also listed in the
+design notes):
+  * Softmax is applied over the routed experts' logits and the selected
+    scores are NOT renormalised (FG Eq. 6–8); the [PS] wording that masks the
+    non-selected logits to -inf before the softmax is not followed.
+  * Softmax is strictly increasing in the logit with a common denominator, so
+    the top mK of the exact scores are the top mK of the logits: the choice
+    is taken on the fp32 logits themselves (exact), ties to the lower index.
+  * The V3 choice key is s_i + b_i taken in fp32, as the kernel takes it:
+    fp32(fp32(sigmoid(z_i)) + b_i), with sigmoid evaluated in float64 and
+    rounded once.  Gate weights use float64 scores.
+  * No FFN biases; SwiGLU is (SiLU(x W1ᵀ) ⊙ x W3ᵀ) W2ᵀ; SiLU(a) = a/(1+e^-a).
+  * An optional per-expert logit offset o_i is added to the logit before
+    scoring (it changes choice and weight alike, unlike b_i).
+  * Dispatch order: permuted rows sorted by expert, then token (each token
+    picks an expert at most once, so slot order never decides).
+
+Weight layout (nn.Linear convention, contracted dimension last):
+  centroids [E, H]; w1, w3 [I, H] per expert; w2 [H, I] per expert.
+"""
+from __future__ import annotations
+
+from math import comb
+from typing import Callable, Optional, Sequence
+
+import numpy as np
+
+SOFTMAX = "softmax"
+SIGMOID_BIAS = "sigmoid_bias"
+RELU = "relu"
+SWIGLU = "swiglu"
+
+
+# --------------------------------------------------------------------------
+# Shapes from the segmentation rule ([FG] §2.1, §3.1)
+# --------------------------------------------------------------------------
+
+def segmented_shape(N: int, M: int, m: int, K: int, Ks: int = 0):
+    """Fine-grained segmentation plus shared isolation, as in [FG] §2.1/§3.1.
+
+    N base experts of width M, K active, split m ways: mN experts of width
+    M/m with mK active; Ks of the mN are made shared (always on), so the
+    router chooses mK - Ks among the remaining mN - Ks.
+    Returns (n_routed, inter, top_k).
+    """
+    if M % m:
+        raise ValueError("M must divide by m")
+    return m * N - Ks, M // m, m * K - Ks
+
+
+def iso_identities(N, M, m, K, Ks, H):
+    """[FG] §2.1: parameters mN·H·(M/m) = N·H·M and active mK·H·(M/m) = K·H·M.
+
+    Counts shared experts inside mN and mK (FG Eq. 9–11 numbers them as part
+    of the mN pool).  Returns ((lhs, rhs) params, (lhs, rhs) active).
+    """
+    n_routed, inter, top_k = segmented_shape(N, M, m, K, Ks)
+    params = ((n_routed + Ks) * H * inter, N * H * M)
+    active = ((top_k + Ks) * H * inter, K * H * M)
+    return params, active
+
+
+def routing_combinations(n_routed: int, top_k: int) -> int:
+    """Number of distinct expert sets a token can pick ([FG] §2.2)."""
+    return comb(n_routed, top_k)
+
+
+# --------------------------------------------------------------------------
+# Router ([FG] Eq. 6–8, Eq. 12–15; [CH7] §7.4)
+# --------------------------------------------------------------------------
+
+def router_logits(u: np.ndarray, centroids: np.ndarray,
+                  logit_offset: Optional[np.ndarray] = None) -> np.ndarray:
+    """z_{t,i} = u_tᵀ e_i (+ o_i), accumulated in float64, rounded to fp32."""
+    z = np.asarray(u, np.float64) @ np.asarray(centroids, np.float64).T
+    if logit_offset is not None:
+        z = z + np.asarray(logit_offset, np.float64)[None, :]
+    return z.astype(np.float32)
+
+
+def softmax_scores(z: np.ndarray) -> np.ndarray:
+    """s_{i,t} = softmax_i(z_{t,i}) over the routed experts, float64."""
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def sigmoid_scores(z: np.ndarray) -> np.ndarray:
+    """s_{i,t} = 1 / (1 + exp(-z_{t,i})), float64 ([FG] Eq. 12)."""
+    z = np.asarray(z, np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def topk_by_rank(key: np.ndarray, k: int) -> np.ndarray:
+    """Top-k by the counting definition, ties to the lower index.
+
+    Expert i's rank is #{j : key_j > key_i} + #{j < i : key_j == key_i};
+    i is chosen iff rank < k, and the output lists the chosen experts by
+    rank (descending key, lower index first on ties).  Returns int64 [T, k].
+    """
+    key = np.asarray(key)
+    T, E = key.shape
+    out = np.empty((T, k), dtype=np.int64)
+    lower = np.tril(np.ones((E, E), dtype=bool), -1)  # lower[i, j] = j < i
+    step = max(1, (1 << 22) // max(1, E * E))
+    for t0 in range(0, T, step):
+        kc = key[t0:t0 + step]
+        ki = kc[:, :, None]   # [c, i, 1]
+        kj = kc[:, None, :]   # [c, 1, j]
+        rank = (kj > ki).sum(axis=2) + ((kj == ki) & lower[None]).sum(axis=2)
+        for c in range(kc.shape[0]):
+            chosen = np.nonzero(rank[c] < k)[0]
+            out[t0 + c, rank[c, chosen]] = chosen
+    return out
+
+
+def selection_key(z: np.ndarray, gate: str,
+                  select_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """The quantity the top-k is taken on (see the module readings)."""
+    if gate == SOFTMAX:
+        return np.asarray(z, np.float32)
+    if gate == SIGMOID_BIAS:
+        s32 = sigmoid_scores(z).astype(np.float32)
+        b = (np.zeros(z.shape[1], np.float32) if select_bias is None
+             else np.asarray(select_bias, np.float32))
+        return s32 + b[None, :]          # fp32 + fp32 -> fp32, one rounding
+    raise ValueError(gate)
+
+
+def route(z: np.ndarray, gate: str, top_k: int,
+          select_bias: Optional[np.ndarray] = None):
+    """Scores, choice and gate weights for every token.
+
+    Returns dict(idx [T,k] int64, weights [T,k] float64, scores [T,E] float64,
+    key [T,E], gap [T] float64).  gap is the k-th minus the (k+1)-th largest
+    score (softmax) or key (sigmoid + bias); +inf when k equals E.
+    """
+    z = np.asarray(z, np.float32)
+    T, E = z.shape
+    scores = softmax_scores(z) if gate == SOFTMAX else sigmoid_scores(z)
+    key = selection_key(z, gate, select_bias)
+    idx = topk_by_rank(key, min(top_k + 1, E))
+    gap = np.full(T, np.inf)
+    if 0 < top_k < E:
+        rows = np.arange(T)
+        gap_src = scores if gate == SOFTMAX else key.astype(np.float64)
+        gap = gap_src[rows, idx[:, top_k - 1]] - gap_src[rows, idx[:, top_k]]
+    idx = idx[:, :top_k]
+    g = np.take_along_axis(scores, idx, axis=1)
+    if gate == SIGMOID_BIAS and top_k > 0:
+        g = g / g.sum(axis=1, keepdims=True)     # [FG] Eq. 15, raw scores only
+    return dict(idx=idx, weights=g, scores=scores, key=key, gap=gap)
+
+
+# --------------------------------------------------------------------------
+# Dispatch (grouping rows by expert; no token is dropped)
+# --------------------------------------------------------------------------
+
+def dispatch(idx: np.ndarray, n_routed: int):
+    """Per-expert counts, offsets and the stable token permutation.
+
+    Rows of the permuted buffer are sorted by expert, then by token; row r
+    holds token row_token[r]; slot_row[t, s] is the row of (token t, slot s).
+    """
+    idx = np.asarray(idx, np.int64)
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    counts = np.bincount(flat, minlength=n_routed).astype(np.int64)
+    offsets = np.zeros(n_routed + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    order = np.argsort(flat, kind="stable")       # (expert, token, slot)
+    row_token = order // max(k, 1)
+    slot_row = np.empty(T * k, np.int64)
+    slot_row[order] = np.arange(T * k)
+    return dict(counts=counts, offsets=offsets, row_token=row_token,
+                slot_row=slot_row.reshape(T, k))
+
+
+# --------------------------------------------------------------------------
+# Expert FFN and combine ([PS]; [FG] Eq. 9–11)
+# --------------------------------------------------------------------------
+
+def silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_ffn(x: np.ndarray, w1: np.ndarray, w2: np.ndarray,
+               w3: Optional[np.ndarray], act: str) -> np.ndarray:
+    """One expert on the rows of x, float64.
+
+    relu:   y = ReLU(x W1ᵀ) W2ᵀ
+    swiglu: y = (SiLU(x W1ᵀ) ⊙ (x W3ᵀ)) W2ᵀ
+    """
+    x = np.asarray(x, np.float64)
+    a = x @ np.asarray(w1, np.float64).T
+    if act == RELU:
+        hmid = np.maximum(a, 0.0)
+    elif act == SWIGLU:
+        hmid = silu(a) * (x @ np.asarray(w3, np.float64).T)
+    else:
+        raise ValueError(act)
+    return hmid @ np.asarray(w2, np.float64).T
+
+
+def combine(u: np.ndarray, y_shared: Sequence[np.ndarray],
+            y_routed: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """h_t = Σ_j y^shared_{j,t} + Σ_s g_{t,s} y_{t,s} + u_t  ([FG] Eq. 9–11).
+
+    y_routed is [T, k, H] (the output of the expert chosen in each slot),
+    weights [T, k].
+    """
+    h = np.asarray(u, np.float64).copy()
+    for ys in y_shared:
+        h += ys
+    if y_routed.shape[1]:
+        h += (np.asarray(weights, np.float64)[:, :, None] * y_routed).sum(axis=1)
+    return h
+
+
+ExpertFn = Callable[[int], tuple]   # e -> (w1, w3 or None, w2) as float64 arrays
+
+
+def layer_forward(u: np.ndarray, route_out: dict, routed: ExpertFn,
+                  shared: ExpertFn, n_shared: int, act: str,
+                  rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """h for the tokens ``rows`` (all tokens if None), float64.
+
+    ``route_out`` is the result of :func:`route` for all tokens; ``routed``
+    and ``shared`` return an expert's weights on demand, so that large layers
+    can be evaluated one expert at a time.
+    """
+    u = np.asarray(u, np.float64)
+    rows = np.arange(u.shape[0]) if rows is None else np.asarray(rows)
+    x = u[rows]
+    idx = route_out["idx"][rows]
+    g = route_out["weights"][rows]
+    n, k = idx.shape
+    y_sh = []
+    for j in range(n_shared):
+        w1, w3, w2 = shared(j)
+        y_sh.append(expert_ffn(x, w1, w2, w3, act))
+    y_r = np.zeros((n, k, u.shape[1]))
+    for e in np.unique(idx):
+        tt, ss = np.nonzero(idx == e)
+        w1, w3, w2 = routed(int(e))
+        y_r[tt, ss] = expert_ffn(x[tt], w1, w2, w3, act)
+    return combine(x, y_sh, y_r, g)
+
+
+def layer_flops(T: int, H: int, inter: int, top_k: int, n_shared: int,
+                act: str) -> int:
+    """Algorithmic expert-FFN FLOPs: every routed row and shared row computed."""
+    mats = 3 if act == SWIGLU else 2
+    return T * (top_k + n_shared) * mats * 2 * H * inter
