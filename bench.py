@@ -1,0 +1,404 @@
+"""Benchmark of the DeepSeekMoE layer forward on B300.
+
+One step = one pass of the whole layer (router logits, route, dispatch,
+expert FFNs, combine) over one batch of T seeded synthetic tokens whose
+inputs are already resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Under torchrun every rank runs an independent replica of the layer on its own
+GPU (tokens are independent, so the layer shards by batch with no exchange);
+value = all tokens processed / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fine_grained_shared_gemm_b300 import moe as M          # noqa: E402
+from fine_grained_shared_gemm_b300 import workloads as W    # noqa: E402
+
+DEFAULT_WORKLOAD = "dsmoe16b_bf16"
+METRIC = "MoE layer tokens/s & TFLOP/s (% bf16 peak); decode weight GB/s (% HBM)"
+L2_FLUSH_BYTES = 512 << 20     # larger than the 126 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def expert_flops(s: W.MoEShape) -> int:
+    return s.T * (s.top_k + s.n_shared) * s.n_mats * 2 * s.H * s.inter
+
+
+def touched_weight_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
+    """Expert weights a step must read at least once: every expert with a token."""
+    used = int((np.diff(offsets) > 0).sum()) + s.n_shared
+    return used * s.n_mats * s.H * s.inter * 2 + s.n_routed * s.H * 2
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "fine_grained_shared_gemm_b300", "csrc", "tc_gemm.cuh")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per expert-FFN call from the committed ncu summary, if it was
+    taken on the current tensor-core kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "expert_ffn_dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload and parts[1] == want:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class Layer:
+    """Device buffers and the five C-ABI calls of one layer step."""
+
+    def __init__(self, shape: W.MoEShape, dev):
+        self.s = s = shape
+        self.inp = W.make_inputs(shape, dev, seed=0)
+        self.wt = M.weights_struct(self.inp)
+        T, E, k, Ks, H = s.T, s.n_routed, s.top_k, s.n_shared, s.H
+        dt = s.torch_dtype
+        self.logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.off = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+        self.row_token = torch.empty((T * k,), dtype=torch.int32, device=dev)
+        self.slot_row = torch.empty((T * k,), dtype=torch.int32, device=dev)
+        self.u_perm = torch.empty((T * k, H), dtype=dt, device=dev)
+        self.y_perm = torch.empty((T * k, H), dtype=dt, device=dev)
+        self.y_shared = torch.empty((Ks, T, H), dtype=dt, device=dev)
+        self.h = torch.empty((T, H), dtype=dt, device=dev)
+        self.ws_d = M.alloc_workspace(M.moe_dispatch_workspace_size(s), dev)
+        self.ws_f = M.alloc_workspace(M.moe_expert_ffn_workspace_size(s), dev)
+        self.ws_l = M.alloc_workspace(M.moe_layer_workspace_size(s), dev)
+        self.launches_per_step = 10
+
+    def step(self, ev=None):
+        s, i = self.s, self.inp
+        M.moe_router_logits(s, i.u, i.centroids, i.logit_offset, self.logits)
+        M.moe_route(s, self.logits, i.select_bias, self.idx, self.w)
+        M.moe_dispatch(s, self.idx, i.u, self.off, self.row_token, self.slot_row, self.u_perm,
+                       self.ws_d)
+        if ev is not None:
+            ev[0].record()
+        M.moe_expert_ffn(s, self.wt, i.u, self.u_perm, self.off, self.y_perm, self.y_shared,
+                         self.ws_f)
+        if ev is not None:
+            ev[1].record()
+        M.moe_combine(s, i.u, self.y_perm, self.y_shared, self.w, self.slot_row, self.h)
+
+
+def run_cuda(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    shape = W.SHAPES[args.workload]
+    layer = Layer(shape, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        layer.step()
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code} after warm-up")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()                       # L2 flushed between timed steps
+            starts[i].record()
+            layer.step(ffn_ev[i])
+            ends[i].record()
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ffn_ms = [a.elapsed_time(b) for a, b in ffn_ev]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    tokens = shape.T * K * world
+    value = tokens / total_s
+
+    # end to end through the host-buffer entry point: H2D of u, layer, D2H of h
+    u_host = layer.inp.u.cpu().pin_memory()
+    h_host = torch.empty_like(u_host).pin_memory()
+    u_dev = torch.empty_like(layer.inp.u)
+    for _ in range(max(1, args.warmup)):
+        M.moe_layer_forward_host(shape, layer.wt, u_host, h_host, u_dev, layer.h, layer.ws_l)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        M.moe_layer_forward_host(shape, layer.wt, u_host, h_host, u_dev, layer.h, layer.ws_l)
+    e1.record()
+    barrier()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code}")
+
+    peaks, peak_src = load_peaks()
+    ffn_avg_s = sum(ffn_ms) / len(ffn_ms) / 1e3
+    flops = expert_flops(shape)
+    offsets = layer.off.cpu().numpy()
+    decode_like = shape.T * shape.top_k < 2 * shape.n_routed
+    if decode_like:
+        alg_bytes = touched_weight_bytes(shape, offsets)
+        achieved = alg_bytes / ffn_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = flops / ffn_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    roof.update({"traffic": recorded_traffic(args.workload), "kernel": "moe_expert_ffn",
+                 "peak_source": f"{peak_src} (burst)", "ms_per_launch": round(ffn_avg_s * 1e3, 4)})
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if shape.dtype == "bf16" else "f32", "data": "synthetic (seeded N(0,1) tokens, "
+        "N(0,1/fan_in) weights)",
+        "config": {"workload": shape.name, "T": shape.T, "H": shape.H,
+                   "n_routed": shape.n_routed, "n_shared": shape.n_shared,
+                   "top_k": shape.top_k, "inter": shape.inter, "gate": shape.gate,
+                   "act": shape.act, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "expert_tflops": round(flops / ffn_avg_s / 1e12, 1),
+        "layer_tflops": round(flops / (total_s / K / world) / 1e12, 1) if world == 1 else None,
+        "roofline": roof,
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(u_host.numel() * u_host.element_size()),
+                "d2h_bytes_per_step": int(h_host.numel() * h_host.element_size())},
+        "gpu_launches": layer.launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, layer, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def _oracle_setup(shape, inp):
+    """Host float64 copies of what the oracle needs (outside any timing)."""
+    import oracle.moe_oracle as O  # the oracle is imported only for this leg
+    np64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    routed = {}
+    shared = [(np64(inp.sw1[j]), None if inp.sw3 is None else np64(inp.sw3[j]),
+               np64(inp.sw2[j])) for j in range(shape.n_shared)]
+
+    def routed_fn(e):
+        if e not in routed:
+            routed[e] = (np64(inp.w1[e]), None if inp.w3 is None else np64(inp.w3[e]),
+                         np64(inp.w2[e]))
+        return routed[e]
+    cents = np64(inp.centroids)
+    off = None if inp.logit_offset is None else np64(inp.logit_offset)
+    bias = None if inp.select_bias is None else inp.select_bias.cpu().numpy()
+    return O, routed_fn, (lambda j: shared[j]), cents, off, bias
+
+
+def _oracle_tokens(O, shape, u_rows, routed_fn, shared_fn, cents, off, bias):
+    z = O.router_logits(u_rows, cents, off)
+    r = O.route(z, shape.gate, shape.top_k, bias)
+    O.dispatch(r["idx"], shape.n_routed)
+    return O.layer_forward(u_rows, r, routed_fn, shared_fn, shape.n_shared, shape.act)
+
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(shape, layer, n_sample):
+    inp = layer.inp
+    O, routed_fn, shared_fn, cents, off, bias = _oracle_setup(shape, inp)
+    rows = np.sort(np.random.default_rng(0).choice(shape.T, size=min(n_sample, shape.T),
+                                                   replace=False))
+    u = inp.u[torch.from_numpy(rows).to(inp.u.device)].to(torch.float64).cpu().numpy()
+    # weights of every expert these tokens use are converted before timing
+    z = O.router_logits(u, cents, off)
+    for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
+        routed_fn(int(e))
+    t0 = time.perf_counter()
+    _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
+    dt = time.perf_counter() - t0
+    return {"value": round(len(rows) / dt, 2), "unit": "tokens/s", "cores": _threads(),
+            "kind": "oracle", "sample": f"{len(rows)} of {shape.T} tokens of {shape.name}, "
+            f"full layer (logits, route, dispatch, FFN, combine) in float64 NumPy; "
+            f"weights pre-converted to float64 outside the timing; {dt:.2f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    shape = W.SHAPES[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_inputs(shape, dev, seed=0)
+    O, routed_fn, shared_fn, cents, off, bias = _oracle_setup(shape, inp)
+    u_all = inp.u
+    n = min(args.cpu_sample, shape.T)
+    rng = np.random.default_rng(1)
+    samples = []
+    for _ in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(shape.T, size=n, replace=False))
+        samples.append(u_all[torch.from_numpy(rows).to(u_all.device)].to(torch.float64).cpu().numpy())
+    for u in samples:       # expert weights resident in host memory before timing
+        z = O.router_logits(u, cents, off)
+        for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
+            routed_fn(int(e))
+    for u in samples[:args.warmup]:
+        _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
+    t0 = time.perf_counter()
+    for u in samples[args.warmup:]:
+        _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "T": shape.T, "H": shape.H,
+                   "n_routed": shape.n_routed, "n_shared": shape.n_shared,
+                   "top_k": shape.top_k, "inter": shape.inter},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": _threads(),
+                         "kind": "oracle", "sample": f"{n} tokens per step of {shape.name}"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.SHAPES))
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

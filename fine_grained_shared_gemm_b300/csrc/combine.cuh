@@ -1,0 +1,51 @@
+// Combine: h_t = u_t + Σ_{j<Ks} y_shared[j, t] + Σ_{s<k} g[t, s] · y_perm[slot_row[t, s]]
+// (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE", §3.1 Eq. 9–11: shared
+// experts, gate-weighted routed experts, residual).  fp32 accumulation in this
+// fixed order and one rounding to the output type, so the result is the same
+// on every run.  One warp per token, 16-byte vectors along H.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(
+    const T* __restrict__ u, const T* __restrict__ y_perm, const T* __restrict__ y_shared,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ slot_row, int n_tokens, int H,
+    int k, int Ks, T* __restrict__ h) {
+  constexpr int V = Vec16<T>::N;
+  __shared__ int s_row[8][32];
+  __shared__ float s_w[8][32];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = H / V;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += warps) {
+    __syncwarp();
+    if (lane < k) {  // k <= 32: slot s's row and weight, broadcast through shared memory
+      s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
+      s_w[wib][lane] = __ldg(topk_w + static_cast<size_t>(t) * k + lane);
+    }
+    __syncwarp();
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[V], y[V];
+      Vec16<T>::load(u + static_cast<size_t>(t) * H + v * V, acc);
+      for (int j = 0; j < Ks; ++j) {
+        Vec16<T>::load(y_shared + (static_cast<size_t>(j) * n_tokens + t) * H + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += y[i];
+      }
+      for (int s = 0; s < k; ++s) {
+        const int row = s_row[wib][s];
+        const float w = s_w[wib][s];
+        if (row < 0) continue;
+        Vec16<T>::load(y_perm + static_cast<size_t>(row) * H + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+      }
+      Vec16<T>::store(h + static_cast<size_t>(t) * H + v * V, acc);
+    }
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,624 @@
+// C-ABI entry points of the MoE layer forward (declared in include/moe.h).
+//
+// Host side only: argument checks, scratch carving, TMA tensor maps and the
+// launches of the kernels in the headers included below.  Nothing here
+// allocates device memory; every launch goes to the caller's stream.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <climits>
+#include <mutex>
+
+#include "moe.h"
+
+#include "combine.cuh"
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "route.cuh"
+#include "simt_gemm.cuh"
+#include "tc_gemm.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+moe_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call)                                \
+  do {                                                \
+    cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_);      \
+  } while (0)
+
+#define MOE_TRY(call)                                 \
+  do {                                                \
+    moe_status s_ = (call);                           \
+    if (s_ != MOE_OK) return s_;                      \
+  } while (0)
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t elt_bytes(const moe_shape* s) { return s->dtype == MOE_DTYPE_F32 ? 4 : 2; }
+inline cudaStream_t cs(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+moe_status check_shape(const moe_shape* s) {
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->H <= 0 || s->n_routed < 1 || s->n_shared < 0 || s->top_k < 0 ||
+      s->inter <= 0 || s->top_k > s->n_routed)
+    return MOE_ERR_INVALID_ARG;
+  if (s->gate != MOE_GATE_SOFTMAX && s->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if (s->act != MOE_ACT_RELU && s->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_DTYPE_F32 && s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (s->n_routed + s->n_shared > 1024 || s->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (s->H % 8 != 0 || s->inter % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->dtype == MOE_DTYPE_BF16) {
+    if (s->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->inter % (s->act == MOE_ACT_SWIGLU ? 64 : 128) != 0) return MOE_ERR_UNSUPPORTED;
+  }
+  const long long rows = static_cast<long long>(s->T) * (s->top_k + s->n_shared);
+  if (rows > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(s->n_routed + s->n_shared) * s->inter > INT_MAX / 2 ||
+      static_cast<long long>(s->n_routed + s->n_shared) * s->H > INT_MAX / 2)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// ---------------------------------------------------------------- TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [rows, cols] row-major, box of 64 columns (128 bytes) x box_rows rows,
+// 128-byte swizzle, zero fill outside the tensor.
+moe_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+// Token-source maps for every box height.
+moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, uint64_t cols) {
+  for (int i = 0; i < tc::kNumBoxes; ++i) MOE_TRY(make_map(&maps[i], base, rows, cols, 16u << i));
+  return MOE_OK;
+}
+
+template <int EPI, int BN>
+moe_status launch_tc(const tc::Params& p, int grid, cudaStream_t st) {
+  using C = tc::Config<BN>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    MOE_CUDA(cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, BN>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  tc::grouped_gemm_kernel<EPI, BN><<<grid, tc::kNumThreads, C::kSmemBytes, st>>>(p);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+template <int EPI>
+moe_status launch_tc_bn(const tc::Params& p, int bn, int grid, cudaStream_t st) {
+  return bn == 256 ? launch_tc<EPI, 256>(p, grid, st) : launch_tc<EPI, 64>(p, grid, st);
+}
+
+// ---------------------------------------------------------------- workspace
+
+struct DispatchWs {
+  int32_t* chunk_hist;
+  int32_t* chunk_base;
+};
+
+size_t dispatch_ws_bytes(const moe_shape* s) {
+  const size_t n = static_cast<size_t>(cdiv(s->T, kDispatchChunk)) * s->n_routed * 4;
+  return 2 * align256(n);
+}
+
+DispatchWs carve_dispatch(void* ws, const moe_shape* s) {
+  const size_t n = static_cast<size_t>(cdiv(s->T, kDispatchChunk)) * s->n_routed * 4;
+  char* p = static_cast<char*>(ws);
+  return DispatchWs{reinterpret_cast<int32_t*>(p), reinterpret_cast<int32_t*>(p + align256(n))};
+}
+
+struct FfnWs {
+  GroupDesc* g1;
+  GroupDesc* g2;
+  int* tile_prefix;
+  void* act;
+};
+
+size_t act_rows(const moe_shape* s) {
+  return static_cast<size_t>(s->T) * (s->top_k + s->n_shared);
+}
+
+size_t ffn_ws_bytes(const moe_shape* s) {
+  const size_t G = s->n_routed + s->n_shared;
+  return 2 * align256(G * sizeof(GroupDesc)) + align256((G + 1) * 4) +
+         align256(act_rows(s) * s->inter * elt_bytes(s));
+}
+
+FfnWs carve_ffn(void* ws, const moe_shape* s) {
+  const size_t G = s->n_routed + s->n_shared;
+  char* p = static_cast<char*>(ws);
+  FfnWs w;
+  w.g1 = reinterpret_cast<GroupDesc*>(p);
+  p += align256(G * sizeof(GroupDesc));
+  w.g2 = reinterpret_cast<GroupDesc*>(p);
+  p += align256(G * sizeof(GroupDesc));
+  w.tile_prefix = reinterpret_cast<int*>(p);
+  p += align256((G + 1) * 4);
+  w.act = p;
+  return w;
+}
+
+struct LayerWs {
+  float* logits;
+  int32_t* idx;
+  float* w;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* slot_row;
+  void* u_perm;
+  void* y_perm;
+  void* y_shared;
+  void* dispatch_ws;
+  void* ffn_ws;
+  size_t total;
+};
+
+LayerWs carve_layer(void* ws, const moe_shape* s) {
+  const size_t T = s->T, E = s->n_routed, k = s->top_k, Ks = s->n_shared, H = s->H;
+  const size_t e = elt_bytes(s);
+  char* base = static_cast<char*>(ws);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base + off;
+    off += align256(bytes);
+    return static_cast<void*>(p);
+  };
+  LayerWs L;
+  L.logits = static_cast<float*>(take(T * E * 4));
+  L.idx = static_cast<int32_t*>(take(T * k * 4));
+  L.w = static_cast<float*>(take(T * k * 4));
+  L.offsets = static_cast<int32_t*>(take((E + 1) * 4));
+  L.row_token = static_cast<int32_t*>(take(T * k * 4));
+  L.slot_row = static_cast<int32_t*>(take(T * k * 4));
+  L.u_perm = take(T * k * H * e);
+  L.y_perm = take(T * k * H * e);
+  L.y_shared = take(Ks * T * H * e);
+  L.dispatch_ws = take(dispatch_ws_bytes(s));
+  L.ffn_ws = take(ffn_ws_bytes(s));
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------- steps
+
+int route_blocks(int T) { return std::max(1, std::min(cdiv(T, 8), num_sms() * 8)); }
+
+moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
+                            const float* off, float* logits, cudaStream_t st) {
+  const int T = s->T, E = s->n_routed, H = s->H;
+  if (T == 0) return MOE_OK;
+  if (s->dtype == MOE_DTYPE_F32) {
+    SimtParams p{};
+    p.a[0] = p.a[1] = static_cast<const float*>(cent);
+    p.b[0] = p.b[1] = static_cast<const float*>(u);
+    p.out[0] = p.out[1] = logits;
+    p.groups = nullptr;
+    p.dense_count = T;
+    p.K = H;
+    p.n_cols = E;
+    p.out_ld = E;
+    p.col_offset = off;
+    dim3 grid(cdiv(E, kSimtTile), cdiv(T, kSimtTile), 1);
+    simt_gemm_kernel<SIMT_LOGITS><<<grid, 256, 0, st>>>(p);
+    MOE_CUDA(cudaGetLastError());
+    return MOE_OK;
+  }
+  tc::Params p;
+  memset(&p, 0, sizeof(p));
+  MOE_TRY(make_map(&p.a[0], cent, E, H, tc::kBM));
+  p.a[1] = p.a[0];
+  p.a3[0] = p.a3[1] = p.a[0];
+  MOE_TRY(make_token_maps(p.b[0], u, T, H));
+  memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+  p.groups = nullptr;
+  p.tile_prefix = nullptr;
+  p.dense_count = T;
+  p.n_wtiles = cdiv(E, tc::kBM);
+  p.num_k_blocks = cdiv(H, tc::kBK);
+  p.out[0] = p.out[1] = logits;
+  p.out_ld = E;
+  p.out_cols = E;
+  p.col_offset = off;
+  const int bn = (T > 64 && p.n_wtiles * cdiv(T, 256) >= num_sms()) ? 256 : 64;
+  const int tiles = p.n_wtiles * cdiv(T, bn);
+  return launch_tc_bn<tc::EPI_F32>(p, bn, std::min(tiles, num_sms()), st);
+}
+
+moe_status do_route(const moe_shape* s, const float* logits, const float* bias, int32_t* idx,
+                    float* w, float* gap, cudaStream_t st) {
+  const int T = s->T, E = s->n_routed;
+  if (T == 0) return MOE_OK;
+  const int blocks = route_blocks(T);
+  const int npl = cdiv(E, 32);
+  const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
+#define MOE_ROUTE(N) route_kernel<N><<<blocks, 256, 0, st>>>(logits, bias, T, E, s->top_k, gate, idx, w, gap)
+  if (npl <= 1) MOE_ROUTE(1);
+  else if (npl <= 2) MOE_ROUTE(2);
+  else if (npl <= 4) MOE_ROUTE(4);
+  else if (npl <= 8) MOE_ROUTE(8);
+  else if (npl <= 16) MOE_ROUTE(16);
+  else MOE_ROUTE(32);
+#undef MOE_ROUTE
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status do_dispatch(const moe_shape* s, const int32_t* idx, const void* u, int32_t* offsets,
+                       int32_t* row_token, int32_t* slot_row, void* u_perm, void* ws,
+                       cudaStream_t st) {
+  const int T = s->T, E = s->n_routed, k = s->top_k;
+  const int n_chunks = cdiv(T, kDispatchChunk);
+  DispatchWs d = carve_dispatch(ws, s);
+  if (n_chunks > 0 && k > 0)
+    dispatch_count<<<n_chunks, 256, E * 4, st>>>(idx, T, k, E, d.chunk_hist);
+  else if (n_chunks > 0)
+    MOE_CUDA(cudaMemsetAsync(d.chunk_hist, 0, static_cast<size_t>(n_chunks) * E * 4, st));
+  MOE_CUDA(cudaGetLastError());
+  dispatch_scan<<<1, 1024, 0, st>>>(d.chunk_hist, n_chunks, E, d.chunk_base, offsets);
+  MOE_CUDA(cudaGetLastError());
+  if (n_chunks == 0 || k == 0) return MOE_OK;
+  dispatch_scatter<<<n_chunks, kDispatchWarps * 32, kDispatchWarps * E * 4, st>>>(
+      idx, T, k, E, d.chunk_base, row_token, slot_row);
+  MOE_CUDA(cudaGetLastError());
+  const int rows = T * k;
+  const int blocks = std::max(1, std::min(cdiv(rows, 8), num_sms() * 16));
+  if (s->dtype == MOE_DTYPE_F32)
+    gather_rows<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(u), T, row_token,
+                                               offsets + E, s->H, static_cast<float*>(u_perm));
+  else
+    gather_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(u), T, row_token, offsets + E, s->H,
+        static_cast<__nv_bfloat16*>(u_perm));
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+// Token tile height for the tensor-core expert GEMMs: wide tiles when experts
+// get many rows, narrow (deeper pipeline) when they get a handful.
+int ffn_bn(const moe_shape* s) {
+  const long long avg = (static_cast<long long>(s->T) * s->top_k) / s->n_routed;
+  return (avg > 48 || (s->n_shared > 0 && s->top_k == 0 && s->T > 64)) ? 256 : 64;
+}
+
+moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* u,
+                         const void* u_perm, const int32_t* offsets, void* y_perm,
+                         void* y_shared, void* ws, cudaStream_t st) {
+  const int T = s->T, E = s->n_routed, Ks = s->n_shared, k = s->top_k, H = s->H,
+            I = s->inter;
+  const int G = E + Ks, Tk = T * k;
+  const int rows_act = static_cast<int>(act_rows(s));
+  if (T == 0 || rows_act == 0) return MOE_OK;
+  FfnWs f = carve_ffn(ws, s);
+  const bool f32 = s->dtype == MOE_DTYPE_F32;
+  const int bn = f32 ? kSimtTile : ffn_bn(s);
+  ffn_plan_kernel<<<1, cdiv(G, 32) * 32, 0, st>>>(offsets, E, Ks, T, Tk, I, H, bn, f.g1, f.g2,
+                                                   f.tile_prefix);
+  MOE_CUDA(cudaGetLastError());
+  const bool swiglu = s->act == MOE_ACT_SWIGLU;
+
+  if (f32) {
+    SimtParams p{};
+    p.a[0] = static_cast<const float*>(wt->w1);
+    p.a[1] = static_cast<const float*>(Ks ? wt->sw1 : wt->w1);
+    p.a3[0] = static_cast<const float*>(swiglu ? wt->w3 : nullptr);
+    p.a3[1] = static_cast<const float*>(swiglu ? (Ks ? wt->sw3 : wt->w3) : nullptr);
+    p.b[0] = static_cast<const float*>(Tk ? u_perm : u);
+    p.b[1] = static_cast<const float*>(u);
+    p.out[0] = p.out[1] = static_cast<float*>(f.act);
+    p.groups = f.g1;
+    p.K = H;
+    p.n_cols = I;
+    p.out_ld = I;
+    dim3 g1(cdiv(I, kSimtTile), cdiv(T, kSimtTile), G);
+    if (swiglu) simt_gemm_kernel<SIMT_SWIGLU><<<g1, 256, 0, st>>>(p);
+    else simt_gemm_kernel<SIMT_RELU><<<g1, 256, 0, st>>>(p);
+    MOE_CUDA(cudaGetLastError());
+    SimtParams q{};
+    q.a[0] = static_cast<const float*>(wt->w2);
+    q.a[1] = static_cast<const float*>(Ks ? wt->sw2 : wt->w2);
+    q.b[0] = q.b[1] = static_cast<const float*>(f.act);
+    q.out[0] = static_cast<float*>(Tk ? y_perm : y_shared);
+    q.out[1] = static_cast<float*>(Ks ? y_shared : y_perm);
+    q.groups = f.g2;
+    q.K = I;
+    q.n_cols = H;
+    q.out_ld = H;
+    dim3 g2(cdiv(H, kSimtTile), cdiv(T, kSimtTile), G);
+    simt_gemm_kernel<SIMT_PLAIN><<<g2, 256, 0, st>>>(q);
+    MOE_CUDA(cudaGetLastError());
+    return MOE_OK;
+  }
+
+  // ---- GEMM1: gate/up projection with the activation fused in the epilogue
+  tc::Params p;
+  memset(&p, 0, sizeof(p));
+  const uint32_t a1_box = swiglu ? tc::kBM / 2 : tc::kBM;
+  MOE_TRY(make_map(&p.a[0], wt->w1, static_cast<uint64_t>(E) * I, H, a1_box));
+  if (Ks) MOE_TRY(make_map(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H, a1_box));
+  else p.a[1] = p.a[0];
+  if (swiglu) {
+    MOE_TRY(make_map(&p.a3[0], wt->w3, static_cast<uint64_t>(E) * I, H, a1_box));
+    if (Ks) MOE_TRY(make_map(&p.a3[1], wt->sw3, static_cast<uint64_t>(Ks) * I, H, a1_box));
+    else p.a3[1] = p.a3[0];
+  } else {
+    p.a3[0] = p.a[0];
+    p.a3[1] = p.a[1];
+  }
+  MOE_TRY(make_token_maps(p.b[1], u, T, H));
+  if (Tk) MOE_TRY(make_token_maps(p.b[0], u_perm, Tk, H));
+  else memcpy(p.b[0], p.b[1], sizeof(p.b[0]));
+  p.groups = f.g1;
+  p.tile_prefix = f.tile_prefix;
+  p.n_groups = G;
+  p.n_wtiles = I / static_cast<int>(a1_box);
+  p.num_k_blocks = cdiv(H, tc::kBK);
+  p.out[0] = p.out[1] = f.act;
+  p.out_ld = I;
+  p.out_cols = I;
+  if (swiglu) MOE_TRY(launch_tc_bn<tc::EPI_SWIGLU>(p, bn, num_sms(), st));
+  else MOE_TRY(launch_tc_bn<tc::EPI_RELU>(p, bn, num_sms(), st));
+
+  // ---- GEMM2: down projection
+  tc::Params q;
+  memset(&q, 0, sizeof(q));
+  MOE_TRY(make_map(&q.a[0], wt->w2, static_cast<uint64_t>(E) * H, I, tc::kBM));
+  if (Ks) MOE_TRY(make_map(&q.a[1], wt->sw2, static_cast<uint64_t>(Ks) * H, I, tc::kBM));
+  else q.a[1] = q.a[0];
+  q.a3[0] = q.a[0];
+  q.a3[1] = q.a[1];
+  MOE_TRY(make_token_maps(q.b[0], f.act, rows_act, I));
+  memcpy(q.b[1], q.b[0], sizeof(q.b[0]));
+  q.groups = f.g2;
+  q.tile_prefix = f.tile_prefix;
+  q.n_groups = G;
+  q.n_wtiles = H / tc::kBM;
+  q.num_k_blocks = cdiv(I, tc::kBK);
+  q.out[0] = Tk ? y_perm : y_shared;
+  q.out[1] = Ks ? y_shared : y_perm;
+  q.out_ld = H;
+  q.out_cols = H;
+  return launch_tc_bn<tc::EPI_BF16>(q, bn, num_sms(), st);
+}
+
+moe_status do_combine(const moe_shape* s, const void* u, const void* y_perm,
+                      const void* y_shared, const float* w, const int32_t* slot_row, void* h,
+                      cudaStream_t st) {
+  const int T = s->T;
+  if (T == 0) return MOE_OK;
+  const int blocks = route_blocks(T);
+  if (s->dtype == MOE_DTYPE_F32)
+    combine_kernel<float><<<blocks, 256, 0, st>>>(
+        static_cast<const float*>(u), static_cast<const float*>(y_perm),
+        static_cast<const float*>(y_shared), w, slot_row, T, s->H, s->top_k, s->n_shared,
+        static_cast<float*>(h));
+  else
+    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(u), static_cast<const __nv_bfloat16*>(y_perm),
+        static_cast<const __nv_bfloat16*>(y_shared), w, slot_row, T, s->H, s->top_k,
+        s->n_shared, static_cast<__nv_bfloat16*>(h));
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+// Pointer checks: required pointers non-null and 16-byte aligned.
+bool ok_ptr(const void* p) { return p != nullptr && al16(p); }
+bool ok_opt(const void* p) { return p == nullptr || al16(p); }
+
+moe_status check_weights_ffn(const moe_shape* s, const moe_weights* w) {
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool sw = s->act == MOE_ACT_SWIGLU;
+  if (!ok_ptr(w->w1) || !ok_ptr(w->w2) || (sw && !ok_ptr(w->w3))) return MOE_ERR_INVALID_ARG;
+  if (s->n_shared > 0 && (!ok_ptr(w->sw1) || !ok_ptr(w->sw2) || (sw && !ok_ptr(w->sw3))))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status layer_forward(const moe_shape* s, const moe_weights* wt, const void* u, void* h,
+                         const moe_route_outputs* ro, void* ws, size_t ws_bytes,
+                         cudaStream_t st) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_weights_ffn(s, wt));
+  if (!ok_ptr(wt->centroids) || !ok_opt(wt->logit_offset) || !ok_opt(wt->select_bias))
+    return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && (!ok_ptr(u) || !ok_ptr(h))) return MOE_ERR_INVALID_ARG;
+  if (ro != nullptr && (!ok_opt(ro->logits) || !ok_opt(ro->topk_idx) || !ok_opt(ro->topk_w) ||
+                        !ok_opt(ro->expert_offsets)))
+    return MOE_ERR_INVALID_ARG;
+  LayerWs L = carve_layer(nullptr, s);
+  if (ws == nullptr || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  L = carve_layer(ws, s);
+  float* logits = (ro && ro->logits) ? ro->logits : L.logits;
+  int32_t* idx = (ro && ro->topk_idx) ? ro->topk_idx : L.idx;
+  float* w = (ro && ro->topk_w) ? ro->topk_w : L.w;
+  int32_t* offsets = (ro && ro->expert_offsets) ? ro->expert_offsets : L.offsets;
+  const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
+  MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, logits, st));
+  MOE_TRY(do_route(s, logits, bias, idx, w, nullptr, st));
+  MOE_TRY(do_dispatch(s, idx, u, offsets, L.row_token, L.slot_row, L.u_perm, L.dispatch_ws, st));
+  MOE_TRY(do_expert_ffn(s, wt, u, L.u_perm, offsets, L.y_perm, L.y_shared, L.ffn_ws, st));
+  return do_combine(s, u, L.y_perm, L.y_shared, w, L.slot_row, h, st);
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+MOE_API const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+MOE_API int moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+MOE_API moe_status moe_device_status(moe_stream_t stream, int32_t* code) {
+  MOE_CUDA(cudaStreamSynchronize(cs(stream)));
+  int v = 0;
+  MOE_CUDA(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)));
+  if (v != 0) {
+    const int zero = 0;
+    MOE_CUDA(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)));
+  }
+  if (code != nullptr) *code = v;
+  if (v & (DEV_ERR_TIMEOUT_PRODUCER | DEV_ERR_TIMEOUT_MMA | DEV_ERR_TIMEOUT_EPILOGUE))
+    return MOE_ERR_TIMEOUT;
+  if (v & DEV_ERR_BAD_EXPERT) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+MOE_API size_t moe_dispatch_workspace_size(const moe_shape* s) {
+  return check_shape(s) == MOE_OK ? dispatch_ws_bytes(s) : 0;
+}
+
+MOE_API size_t moe_expert_ffn_workspace_size(const moe_shape* s) {
+  return check_shape(s) == MOE_OK ? ffn_ws_bytes(s) : 0;
+}
+
+MOE_API size_t moe_layer_workspace_size(const moe_shape* s) {
+  return check_shape(s) == MOE_OK ? carve_layer(nullptr, s).total : 0;
+}
+
+MOE_API moe_status moe_router_logits(const moe_shape* s, const void* u, const void* centroids,
+                                     const float* logit_offset, float* logits,
+                                     moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_ptr(centroids) || !ok_opt(logit_offset)) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && (!ok_ptr(u) || !ok_ptr(logits))) return MOE_ERR_INVALID_ARG;
+  return do_router_logits(s, u, centroids, logit_offset, logits, cs(stream));
+}
+
+MOE_API moe_status moe_route(const moe_shape* s, const float* logits, const float* select_bias,
+                             int32_t* topk_idx, float* topk_w, float* kth_gap,
+                             moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_opt(select_bias) || !ok_opt(kth_gap)) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && !ok_ptr(logits)) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && s->top_k > 0 && (!ok_ptr(topk_idx) || !ok_ptr(topk_w)))
+    return MOE_ERR_INVALID_ARG;
+  const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? select_bias : nullptr;
+  return do_route(s, logits, bias, topk_idx, topk_w, kth_gap, cs(stream));
+}
+
+MOE_API moe_status moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const void* u,
+                                int32_t* expert_offsets, int32_t* row_token, int32_t* slot_row,
+                                void* u_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_ptr(expert_offsets)) return MOE_ERR_INVALID_ARG;
+  if (s->top_k > 0 && s->T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(u) || !ok_ptr(row_token) ||
+                                   !ok_ptr(slot_row) || !ok_ptr(u_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < dispatch_ws_bytes(s) || (dispatch_ws_bytes(s) > 0 && (ws == nullptr || !al16(ws))))
+    return MOE_ERR_WORKSPACE;
+  return do_dispatch(s, topk_idx, u, expert_offsets, row_token, slot_row, u_perm, ws,
+                     cs(stream));
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_shape* s, const moe_weights* weights, const void* u,
+                                  const void* u_perm, const int32_t* expert_offsets,
+                                  void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_weights_ffn(s, weights));
+  if (!ok_ptr(expert_offsets)) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && !ok_ptr(u)) return MOE_ERR_INVALID_ARG;
+  if (s->top_k > 0 && s->T > 0 && (!ok_ptr(u_perm) || !ok_ptr(y_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (s->n_shared > 0 && s->T > 0 && !ok_ptr(y_shared)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || !al16(ws) || ws_bytes < ffn_ws_bytes(s)) return MOE_ERR_WORKSPACE;
+  return do_expert_ffn(s, weights, u, u_perm, expert_offsets, y_perm, y_shared, ws, cs(stream));
+}
+
+MOE_API moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,
+                               const void* y_shared, const float* topk_w,
+                               const int32_t* slot_row, void* h, moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (s->T > 0 && (!ok_ptr(u) || !ok_ptr(h))) return MOE_ERR_INVALID_ARG;
+  if (s->top_k > 0 && s->T > 0 && (!ok_ptr(y_perm) || !ok_ptr(topk_w) || !ok_ptr(slot_row)))
+    return MOE_ERR_INVALID_ARG;
+  if (s->n_shared > 0 && s->T > 0 && !ok_ptr(y_shared)) return MOE_ERR_INVALID_ARG;
+  return do_combine(s, u, y_perm, y_shared, topk_w, slot_row, h, cs(stream));
+}
+
+MOE_API moe_status moe_layer_forward(const moe_shape* s, const moe_weights* weights,
+                                     const void* u, void* h, const moe_route_outputs* route_out,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return layer_forward(s, weights, u, h, route_out, ws, ws_bytes, cs(stream));
+}
+
+MOE_API moe_status moe_layer_forward_host(const moe_shape* s, const moe_weights* weights,
+                                          const void* u_host, void* h_host, void* u_dev,
+                                          void* h_dev, void* ws, size_t ws_bytes,
+                                          moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (s->T > 0 && (u_host == nullptr || h_host == nullptr || !ok_ptr(u_dev) || !ok_ptr(h_dev)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(s->T) * s->H * elt_bytes(s);
+  cudaStream_t st = cs(stream);
+  if (bytes) MOE_CUDA(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, st));
+  MOE_TRY(layer_forward(s, weights, u_dev, h_dev, nullptr, ws, ws_bytes, st));
+  if (bytes) MOE_CUDA(cudaMemcpyAsync(h_host, h_dev, bytes, cudaMemcpyDeviceToHost, st));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,507 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
+// for the expert FFNs and the router logits of the MoE layer.
+//
+// Orientation ("swap-AB"): the weight rows are the MMA's M side (128 rows per
+// tile) and the token rows are its N side.  The ragged number of tokens each
+// expert receives then only sets N, which the tensor core takes in steps of
+// 16, so a partly filled expert costs little extra work; decode-sized groups
+// of one or two tokens run at N = 16 while the weights stream at full width.
+//
+//   D[j, c] = Σ_k W[j, k] · X[c, k]      (j: weight row, c: token of the group)
+//
+// Both operands are K-major in global memory (nn.Linear weights [out, in] and
+// token rows [T, H]), land in shared memory through TMA with the 128-byte
+// swizzle, and the fp32 accumulator lives in tensor memory (TMEM), double
+// buffered so the epilogue of one tile overlaps the MMAs of the next.
+//
+// Roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocation and MMA issue (one thread)
+//   warps 2..5  epilogue: TMEM -> registers -> shared-memory transpose ->
+//               global, with the FFN activation fused in
+//
+// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets a bit of the
+// device error word, lets every role leave its loop, waits for its own copies
+// and MMAs in flight, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int kBK = 64;            // contraction elements per stage: one 128-byte swizzle row
+constexpr int kBM = 128;           // MMA M (weight rows per tile)
+constexpr int kUmmaK = 16;         // K of one tcgen05.mma for 16-bit inputs
+constexpr int kNumThreads = 192;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
+constexpr int kStageBufFloats = 4 * 32 * 33;
+
+enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
+
+struct Params {
+  CUtensorMap a[2];              // weight stacks (routed, shared)
+  CUtensorMap a3[2];             // SwiGLU up-projection stacks
+  CUtensorMap b[2][kNumBoxes];   // token sources x box heights
+  const GroupDesc* groups;       // [n_groups], or null for one dense group
+  const int* tile_prefix;        // [n_groups + 1] prefix sum of token tiles
+  int n_groups;
+  int dense_count;               // token rows of the dense group
+  int n_wtiles;                  // weight tiles per group
+  int num_k_blocks;              // ceil(K / kBK)
+  void* out[2];
+  int out_ld;                    // output row pitch in elements
+  int out_cols;                  // valid output columns (EPI_F32)
+  const float* col_offset;       // EPI_F32: per-column addend, may be null
+};
+
+template <int BN>
+struct Config {
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (196608 / kStageBytes) > 12 ? 12 : (196608 / kStageBytes);
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kBarBytes + kStageBufFloats * 4;
+  static_assert(kStages >= 2, "pipeline too shallow");
+  static_assert(2 * kStages + 5 <= kBarBytes / 8 - 1, "barrier area too small");
+  static_assert(kSmemBytes <= 232448, "shared memory over the sm_100-family limit");
+};
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// Waits for the phase of the given parity to complete; false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core-matrix groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>(1) << 16) |              // leading offset (unused when swizzled)
+         (static_cast<uint64_t>(1024 >> 4) << 32) |      // stride offset between 8-row groups
+         (static_cast<uint64_t>(1) << 46) |              // descriptor version
+         (static_cast<uint64_t>(2) << 61);               // 128-byte swizzle
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+  // The wait names the registers so that no use of them is scheduled before it.
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+        "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]),
+        "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]),
+        "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]),
+        "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]),
+        "+r"(v[31])
+      :
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the AND of `pred` over the participants.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------------ tiles
+
+struct Tile {
+  int a_sel, a_row, a3_row;
+  int b_src, b_row;
+  int out_sel, out_row, out_col;
+  int n_valid;
+};
+
+__device__ __forceinline__ int box_index(int n) {
+  return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : n <= 128 ? 3 : 4;
+}
+
+template <int EPI, int BN>
+__device__ __forceinline__ Tile decode_tile(const Params& p, int t) {
+  const int nw = p.n_wtiles;
+  GroupDesc d;
+  int nt, local;
+  if (p.groups == nullptr) {
+    d = GroupDesc{0, 0, 0, 0, 0, 0, p.dense_count, 0};
+    nt = (p.dense_count + BN - 1) / BN;
+    local = t;
+  } else {
+    int lo = 0, hi = p.n_groups;  // largest g with prefix[g] * nw <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_prefix + mid) * nw <= t) lo = mid; else hi = mid;
+    }
+    d = p.groups[lo];
+    const int pre = __ldg(p.tile_prefix + lo);
+    nt = __ldg(p.tile_prefix + lo + 1) - pre;
+    local = t - pre * nw;
+  }
+  const int w = local / nt, n = local - w * nt;
+  Tile tl;
+  constexpr int kRowsPerW = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;
+  tl.a_sel = d.a_sel;
+  tl.a_row = d.a_row0 + w * kRowsPerW;
+  tl.a3_row = tl.a_row;
+  tl.b_src = d.b_src;
+  tl.b_row = d.b_row0 + n * BN;
+  tl.out_sel = d.out_sel;
+  tl.out_row = d.out_row0 + n * BN;
+  tl.out_col = w * kRowsPerW;
+  tl.n_valid = min(BN, d.count - n * BN);
+  return tl;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int EPI, int BN>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ Params p) {
+  using C = Config<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar0 = base + S * C::kStageBytes;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
+  float* stage_buf = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 2; ++i) {
+      prefetch_map(&p.a[i]);
+      if (EPI == EPI_SWIGLU) prefetch_map(&p.a3[i]);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int tiles_per_w = (p.groups == nullptr) ? (p.dense_count + BN - 1) / BN
+                                                : __ldg(p.tile_prefix + p.n_groups);
+  const int total = p.n_wtiles * tiles_per_w;
+  const int nk = p.num_k_blocks;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<EPI, BN>(p, t);
+        const int box = box_index(tl.n_valid);
+        const uint32_t bytes = kABytes + (16u << box) * (kBK * 2);
+        const CUtensorMap* bmap = &p.b[tl.b_src][box];
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
+            raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          armed |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sa, &p.a[tl.a_sel], full_bar(stage), kb * kBK, tl.a_row);
+            tma_load_2d(sa + kABytes / 2, &p.a3[tl.a_sel], full_bar(stage), kb * kBK, tl.a3_row);
+          } else {
+            tma_load_2d(sa, &p.a[tl.a_sel], full_bar(stage), kb * kBK, tl.a_row);
+          }
+          tma_load_2d(sa + kABytes, bmap, full_bar(stage), kb * kBK, tl.b_row);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+      // No copy may land after the CTA exits: wait for the last one per stage.
+      for (int s = 0; s < S; ++s)
+        if ((armed >> s) & 1u)
+          if (!mbar_wait(full_bar(s), (last_parity >> s) & 1u))
+            raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<EPI, BN>(p, t);
+        const uint32_t n_mma = (static_cast<uint32_t>(tl.n_valid) + 15u) & ~15u;
+        const uint32_t idesc = idesc_bf16(kBM, n_mma);
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1)) {
+          raise_device_error(DEV_ERR_TIMEOUT_MMA);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase)) {
+            raise_device_error(DEV_ERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * C::kStageBytes;
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            tc_mma(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          tc_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // All MMAs issued by this thread complete before TMEM is freed.
+      tc_commit(done_bar);
+      if (!mbar_wait(done_bar, 0)) raise_device_error(DEV_ERR_TIMEOUT_MMA);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // the TMEM lane quarter this warp may read
+    float* buf = stage_buf + q * 32 * 33;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<EPI, BN>(p, t);
+      const bool ready = mbar_wait(tfull_bar(acc), acc_phase);
+      // all four epilogue warps leave together, so no named barrier is left half-arrived
+      if (!named_bar_and(1, 128, ready)) {
+        if (!ready) raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) +
+                            (static_cast<uint32_t>(q * 32) << 16);
+      for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tacc + c0, v);
+        const bool row_ok = c0 + lane < tl.n_valid;
+        const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
+        if (EPI == EPI_SWIGLU) {
+          // lanes 0..63 hold the gate rows, 64..127 the matching up rows
+          if (q >= 2) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]);
+          }
+          named_bar_sync(1, 128);
+          if (q < 2) {
+            const float* up = stage_buf + (q + 2) * 32 * 33;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(v[i]);
+              const float silu = __fdividef(g, 1.0f + __expf(-g));
+              buf[i * 33 + lane] = silu * up[i * 33 + lane];
+            }
+            __syncwarp();
+            if (row_ok) {
+              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
+                                 orow * p.out_ld + tl.out_col + q * 32;
+              float r[8];
+#pragma unroll
+              for (int j0 = 0; j0 < 32; j0 += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = buf[lane * 33 + j0 + j];
+                Vec16<__nv_bfloat16>::store(o + j0, r);
+              }
+            }
+          }
+          named_bar_sync(1, 128);
+        } else if (EPI == EPI_F32) {
+          const int col = tl.out_col + q * 32 + lane;
+          const float add =
+              (p.col_offset != nullptr && col < p.out_cols) ? __ldg(p.col_offset + col) : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]) + add;
+          __syncwarp();
+          if (row_ok) {
+            float* o = static_cast<float*>(p.out[tl.out_sel]) + orow * p.out_ld;
+            const int c_begin = tl.out_col + q * 32;
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j)
+              if (c_begin + j < p.out_cols) o[c_begin + j] = buf[lane * 33 + j];
+          }
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x = __uint_as_float(v[i]);
+            if (EPI == EPI_RELU) x = fmaxf(x, 0.0f);
+            buf[i * 33 + lane] = x;
+          }
+          __syncwarp();
+          if (row_ok) {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
+                               orow * p.out_ld + tl.out_col + q * 32;
+            float r[8];
+#pragma unroll
+            for (int j0 = 0; j0 < 32; j0 += 8) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) r[j] = buf[lane * 33 + j0 + j];
+              Vec16<__nv_bfloat16>::store(o + j0, r);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+}  // namespace tc
+}  // namespace moe

@@ -1,0 +1,198 @@
+/*
+ * moe.h — C ABI of the B300 (sm_103a) DeepSeekMoE layer forward.
+ *
+ * The layer computed here (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE",
+ * llm-infra-atlas, §3.1 Eq. 9–11; DeepSeek-V3 form Eq. 12–15):
+ *
+ *   h_t = Σ_{j<Ks} FFN_j^shared(u_t) + Σ_{i routed} g_{i,t} · FFN_i(u_t) + u_t
+ *
+ * with fine-grained segmentation (§2.1: mN experts of width M/m, mK active)
+ * and shared-expert isolation (§3.1: Ks always-on experts, routed top-k is
+ * mK − Ks).  Two gates are supported:
+ *   MOE_GATE_SOFTMAX       s = softmax over the routed logits, g = s for the
+ *                          chosen experts, not renormalised (§2.1 Eq. 6–8);
+ *   MOE_GATE_SIGMOID_BIAS  s = sigmoid(logit); the choice is taken on s + b_i
+ *                          (b_i used for the choice only, page "MoE 的分水岭",
+ *                          ibossgateway ch. 7 §7.4); g = s / Σ_chosen s
+ *                          (§3.1 Eq. 12–15).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *    two host pointers of moe_layer_forward_host.  The library allocates
+ *    nothing: scratch comes from the caller through `ws`/`ws_bytes`, sized by
+ *    the matching *_workspace_size function, 256-byte aligned.
+ *  - Layouts are dense row-major.  Weights follow the nn.Linear convention
+ *    (output rows, contracted dimension contiguous):
+ *      centroids [E, H];  w1, w3 [E, I, H];  w2 [E, H, I];
+ *      sw1, sw3 [Ks, I, H];  sw2 [Ks, H, I];  w3 / sw3 are NULL for ReLU.
+ *    Tokens u and outputs h are [T, H].  Element type of u, weights,
+ *    centroids, permuted rows and h is shape->dtype (fp32 or bf16); logits,
+ *    gate weights, biases and offsets are always fp32; indices are int32.
+ *  - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns without synchronising.  Arguments are
+ *    checked on the host before anything is launched; a failed check
+ *    launches nothing.  Errors are returned, never thrown.
+ *  - The expert routing of one token never drops a token (no capacity
+ *    factor; §4 "No token-dropping").
+ *
+ * Limits: 1 ≤ n_routed + n_shared ≤ 1024; 0 ≤ top_k ≤ min(32, n_routed);
+ * H % 8 == 0 and inter % 8 == 0.  bf16 additionally needs H % 128 == 0 and
+ * inter % 64 (SwiGLU) or inter % 128 (ReLU) == 0; otherwise
+ * MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_API __attribute__((visibility("default")))
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL where a pointer is required, bad sizes/enums, misalignment */
+  MOE_ERR_UNSUPPORTED = 2, /* valid layer, but outside this build's kernel limits (see above) */
+  MOE_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes below the *_workspace_size value */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed; see moe_last_cuda_error() */
+  MOE_ERR_TIMEOUT = 5      /* a kernel's bounded wait expired (reported by moe_device_status) */
+} moe_status;
+
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_BIAS = 1 } moe_gate;
+typedef enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* One layer's shape.  T tokens of hidden size H; n_routed routed experts of
+ * which top_k are chosen per token; n_shared always-on experts; every expert
+ * has intermediate width `inter` (M/m in the segmentation notation). */
+typedef struct {
+  int32_t T, H, n_routed, n_shared, top_k, inter;
+  int32_t gate;  /* moe_gate */
+  int32_t act;   /* moe_act */
+  int32_t dtype; /* moe_dtype */
+} moe_shape;
+
+/* Layer parameters (device pointers).  logit_offset [E] (may be NULL) is
+ * added to the logit before scoring and so changes choice and weight alike;
+ * select_bias [E] (may be NULL; ignored by the softmax gate) changes only the
+ * choice. */
+typedef struct {
+  const void* centroids;
+  const float* logit_offset;
+  const float* select_bias;
+  const void *w1, *w3, *w2;
+  const void *sw1, *sw3, *sw2;
+} moe_weights;
+
+/* Optional routing outputs of moe_layer_forward (each may be NULL). */
+typedef struct {
+  float* logits;           /* [T, E] */
+  int32_t* topk_idx;       /* [T, top_k] */
+  float* topk_w;           /* [T, top_k] */
+  int32_t* expert_offsets; /* [E + 1] */
+} moe_route_outputs;
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(int status);
+
+/* cudaError_t of the most recent MOE_ERR_CUDA returned on this host thread
+ * (0 if none). */
+MOE_API int moe_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears this device's error word,
+ * which kernels set when a bounded wait expires (no kernel traps or hangs).
+ * *code receives the raw word (0 = clean).  Returns MOE_ERR_TIMEOUT if the
+ * word was set, MOE_ERR_CUDA if the synchronisation failed, else MOE_OK. */
+MOE_API moe_status moe_device_status(moe_stream_t stream, int32_t* code);
+
+/* Scratch sizes in bytes (0 is a valid answer; an invalid shape returns 0). */
+MOE_API size_t moe_dispatch_workspace_size(const moe_shape* shape);
+MOE_API size_t moe_expert_ffn_workspace_size(const moe_shape* shape);
+MOE_API size_t moe_layer_workspace_size(const moe_shape* shape);
+
+/* Router logits z[t, i] = u_tᵀ e_i (+ logit_offset[i]), fp32 accumulation
+ * (page "02 · 细粒度 MoE", §2.1 Eq. 8: the score is a function of u_tᵀ e_i).
+ * u [T, H], centroids [E, H] in shape->dtype; logits [T, E] fp32 out. */
+MOE_API moe_status moe_router_logits(const moe_shape* shape, const void* u,
+                                     const void* centroids,
+                                     const float* logit_offset, float* logits,
+                                     moe_stream_t stream);
+
+/* Scores, top-k choice and gate weights per token from fp32 logits
+ * (§2.1 Eq. 6–8 for softmax; §3.1 Eq. 12–15 and ch. 7 §7.4 for sigmoid+bias).
+ * The choice is ordered by descending key, ties to the lower expert index;
+ * the softmax key is the logit itself (softmax is increasing in it), the
+ * sigmoid key is fp32(sigmoid(z)) + b_i.  topk_idx [T, top_k] int32 and
+ * topk_w [T, top_k] fp32 out; kth_gap [T] (may be NULL) receives the k-th
+ * minus the (k+1)-th largest score (softmax) or key (sigmoid+bias), +inf if
+ * top_k == E.  select_bias may be NULL. */
+MOE_API moe_status moe_route(const moe_shape* shape, const float* logits,
+                             const float* select_bias, int32_t* topk_idx,
+                             float* topk_w, float* kth_gap,
+                             moe_stream_t stream);
+
+/* Groups token rows by expert (no dropping).  expert_offsets [E + 1] out
+ * (exclusive prefix sum of per-expert counts); permuted rows are sorted by
+ * expert, then token; row_token [T·k] out (token of each permuted row);
+ * slot_row [T·k] out (row of token t's slot s at t·k + s); u_perm [T·k, H]
+ * out, u_perm[r] = u[row_token[r]].  Deterministic (no order-dependent
+ * atomics).  An expert index outside [0, E) sets the device error word and
+ * that entry is skipped.  ws: moe_dispatch_workspace_size bytes. */
+MOE_API moe_status moe_dispatch(const moe_shape* shape, const int32_t* topk_idx,
+                                const void* u, int32_t* expert_offsets,
+                                int32_t* row_token, int32_t* slot_row,
+                                void* u_perm, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/* Expert FFNs over routed and shared experts (page "19-deepseek-moe",
+ * ai.tomabc.com: an expert is ReLU(x W1ᵀ) W2ᵀ without biases; SwiGLU form
+ * (SiLU(x W1ᵀ) ⊙ x W3ᵀ) W2ᵀ).  Routed expert e runs on permuted rows
+ * [expert_offsets[e], expert_offsets[e+1]) of u_perm and writes the same rows
+ * of y_perm [T·k, H]; shared expert j runs on all rows of u and writes
+ * y_shared [Ks, T, H].  Only the w1/w3/w2/sw1/sw3/sw2 members of `weights`
+ * are read.  fp32 accumulation; bf16 layers round the intermediate
+ * activation and the outputs to bf16.  ws: moe_expert_ffn_workspace_size. */
+MOE_API moe_status moe_expert_ffn(const moe_shape* shape,
+                                  const moe_weights* weights, const void* u,
+                                  const void* u_perm,
+                                  const int32_t* expert_offsets, void* y_perm,
+                                  void* y_shared, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* h_t = u_t + Σ_{j<Ks} y_shared[j, t] + Σ_{s<k} topk_w[t, s] · y_perm[slot_row[t, s]]
+ * (§3.1 Eq. 9–11), accumulated in fp32 in exactly this order and rounded
+ * once to shape->dtype.  h [T, H] out; h may not alias any input. */
+MOE_API moe_status moe_combine(const moe_shape* shape, const void* u,
+                               const void* y_perm, const void* y_shared,
+                               const float* topk_w, const int32_t* slot_row,
+                               void* h, moe_stream_t stream);
+
+/* Whole layer: router logits, route, dispatch, expert FFNs, combine, all on
+ * `stream`.  route_out (may be NULL) receives copies of the routing
+ * intermediates.  ws: moe_layer_workspace_size bytes. */
+MOE_API moe_status moe_layer_forward(const moe_shape* shape,
+                                     const moe_weights* weights, const void* u,
+                                     void* h, const moe_route_outputs* route_out,
+                                     void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
+/* The same layer with HOST token buffers: copies u_host [T, H] into u_dev,
+ * runs moe_layer_forward, copies h_dev into h_host [T, H], all on `stream`,
+ * and returns without synchronising (synchronise before reading h_host).
+ * Host buffers should be pinned for the copies to be asynchronous. */
+MOE_API moe_status moe_layer_forward_host(const moe_shape* shape,
+                                          const moe_weights* weights,
+                                          const void* u_host, void* h_host,
+                                          void* u_dev, void* h_dev, void* ws,
+                                          size_t ws_bytes,
+                                          moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,111 @@
+"""The C-ABI library loads without a GPU, exports every entry point declared
+in include/moe.h, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fine_grained_shared_gemm_b300 import moe as M
+from fine_grained_shared_gemm_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    for n in ("moe_router_logits", "moe_route", "moe_dispatch", "moe_expert_ffn",
+              "moe_combine", "moe_layer_forward", "moe_layer_forward_host",
+              "moe_layer_workspace_size", "moe_device_status", "moe_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = M.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in M._SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_only_declared_symbols_are_exported():
+    out = os.popen(f"nm -D --defined-only {M.library_path()}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    moe_syms = {s for s in exported if s.startswith("moe_")}
+    assert moe_syms == set(declared_symbols())
+
+
+def test_status_strings():
+    lib = M.lib()
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(M.MOE_ERR_WORKSPACE).startswith(b"workspace")
+    assert lib.moe_status_string(99) == b"unknown status"
+
+
+def _shape(**kw):
+    base = dict(T=100, H=256, n_routed=16, n_shared=1, top_k=4, inter=128,
+                gate=0, act=1, dtype=1)
+    base.update(kw)
+    return M.moe_shape(**base)
+
+
+def test_workspace_sizes_cover_the_buffers():
+    for name in ("tiny_f32", "dsmoe16b_bf16", "v3_prefill_bf16", "decode_bf16", "sweep_m16"):
+        s = W.SHAPES[name]
+        st = M.shape_struct(s)
+        e = 4 if s.dtype == "f32" else 2
+        lay = M.lib().moe_layer_workspace_size(ctypes.byref(st))
+        # permuted rows in and out plus shared outputs and the intermediate activation
+        need = (2 * s.T * s.top_k * s.H + s.n_shared * s.T * s.H
+                + s.T * (s.top_k + s.n_shared) * s.inter) * e
+        assert lay >= need
+        assert M.lib().moe_expert_ffn_workspace_size(ctypes.byref(st)) >= \
+            s.T * (s.top_k + s.n_shared) * s.inter * e
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(top_k=17), M.MOE_ERR_INVALID_ARG),        # k > E
+    (dict(T=-1), M.MOE_ERR_INVALID_ARG),
+    (dict(H=0), M.MOE_ERR_INVALID_ARG),
+    (dict(gate=7), M.MOE_ERR_INVALID_ARG),
+    (dict(dtype=3), M.MOE_ERR_INVALID_ARG),
+    (dict(n_routed=1100), M.MOE_ERR_UNSUPPORTED),  # E + Ks > 1024
+    (dict(n_routed=64, top_k=33), M.MOE_ERR_UNSUPPORTED),
+    (dict(H=200), M.MOE_ERR_UNSUPPORTED),            # bf16 needs H % 128
+    (dict(inter=96), M.MOE_ERR_UNSUPPORTED),         # bf16 SwiGLU needs inter % 64
+])
+def test_bad_shapes_rejected_on_host(bad, code):
+    s = _shape(**bad)
+    assert M.lib().moe_layer_workspace_size(ctypes.byref(s)) == 0
+    st = M.lib().moe_route(ctypes.byref(s), 256, None, 256, 256, None, None)
+    assert st == code
+
+
+def test_null_and_misaligned_pointers_rejected():
+    s = _shape()
+    L = M.lib()
+    assert L.moe_route(ctypes.byref(s), None, None, 256, 256, None, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ctypes.byref(s), 258, None, 256, 256, None, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(s), 256, 256, None, 256, 256, 256, None) == \
+        M.MOE_ERR_INVALID_ARG   # n_shared = 1 needs y_shared
+    w = M.moe_weights(256, None, None, 256, None, 256, 256, 256, 256)  # SwiGLU without w3
+    assert L.moe_expert_ffn(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, 256, 256,
+                            256, 1 << 30, None) == M.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_too_small_rejected():
+    s = _shape()
+    L = M.lib()
+    w = M.moe_weights(256, None, None, 256, 256, 256, 256, 256, 256)
+    need = L.moe_layer_workspace_size(ctypes.byref(s))
+    assert L.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), 256, 256, None, 256,
+                               need - 1, None) == M.MOE_ERR_WORKSPACE
+    assert L.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), 256, 256, None, None,
+                               need, None) == M.MOE_ERR_WORKSPACE
+    need_d = L.moe_dispatch_workspace_size(ctypes.byref(s))
+    assert L.moe_dispatch(ctypes.byref(s), 256, 256, 256, 256, 256, 256, 256, need_d - 1,
+                          None) == M.MOE_ERR_WORKSPACE
