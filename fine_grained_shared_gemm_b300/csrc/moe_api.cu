@@ -621,4 +621,55 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* s, const moe_weights*
   return MOE_OK;
 }
 
+// ---- moe_dispatch_static: dispatch with its scratch in a fixed array of the
+// library, for callers that cannot hand the library any device memory.
+// 2 x 131072 int32 = 1 MiB: chunk histograms and chunk bases of dispatch.
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kStaticDispatchEntries = 131072;  // ceil(T / 256) * n_routed
+static __device__ __align__(256) int32_t g_static_dispatch_scratch[2 * kStaticDispatchEntries];
+
+// Device address of the array on the current device, looked up once per
+// device.  Host code cannot use the symbol itself as a device pointer.
+moe_status static_dispatch_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    MOE_CUDA(cudaGetSymbolAddress(&p, g_static_dispatch_scratch));
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+MOE_API moe_status moe_dispatch_static(const moe_shape* s, const int32_t* topk_idx,
+                                       const void* u, int32_t* expert_offsets,
+                                       int32_t* row_token, int32_t* slot_row, void* u_perm,
+                                       moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_ptr(expert_offsets)) return MOE_ERR_INVALID_ARG;
+  if (s->top_k > 0 && s->T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(u) || !ok_ptr(row_token) ||
+                                   !ok_ptr(slot_row) || !ok_ptr(u_perm)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t entries = static_cast<size_t>(cdiv(s->T, kDispatchChunk)) * s->n_routed;
+  if (entries > kStaticDispatchEntries) return MOE_ERR_UNSUPPORTED;
+  // Both scratch arrays are fully written by the count and scan kernels (or
+  // the memset for top_k == 0) before they are read: nothing needs clearing.
+  void* scratch = nullptr;
+  MOE_TRY(static_dispatch_scratch(&scratch));
+  return do_dispatch(s, topk_idx, u, expert_offsets, row_token, slot_row, u_perm, scratch,
+                     cs(stream));
+}
+
 }  // extern "C"

@@ -71,6 +71,7 @@ _SIGNATURES = {
     "moe_layer_forward": (ctypes.c_int, [_S, _W, _P, _P, ctypes.POINTER(moe_route_outputs),
                                          _P, ctypes.c_size_t, _P]),
     "moe_layer_forward_host": (ctypes.c_int, [_S, _W, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_dispatch_static": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -169,6 +170,15 @@ def moe_dispatch(shape, topk_idx, u, expert_offsets, row_token, slot_row, u_perm
         ctypes.byref(shape_struct(shape)), _ptr(topk_idx), _ptr(u), _ptr(expert_offsets),
         _ptr(row_token), _ptr(slot_row), _ptr(u_perm), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_dispatch_static(shape, topk_idx, u, expert_offsets, row_token, slot_row, u_perm,
+                        stream=None):
+    """moe_dispatch for callers that cannot provide device scratch: the library
+    uses its own fixed array (see include/moe.h for the size limit)."""
+    _check("moe_dispatch_static", lib().moe_dispatch_static(
+        ctypes.byref(shape_struct(shape)), _ptr(topk_idx), _ptr(u), _ptr(expert_offsets),
+        _ptr(row_token), _ptr(slot_row), _ptr(u_perm), _stream(stream)))
 
 
 def moe_expert_ffn(shape, weights: moe_weights, u, u_perm, expert_offsets, y_perm, y_shared,

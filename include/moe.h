@@ -192,6 +192,29 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* shape,
                                           size_t ws_bytes,
                                           moe_stream_t stream);
 
+/* moe_dispatch without a workspace argument, for callers that cannot
+ * allocate device memory: a runtime whose allocator already owns all of the
+ * GPU's memory and has no scratch to lend, or a latency-critical path that
+ * must not call cudaMalloc (it can synchronise the device).  The source pages
+ * have no counterpart; this is a deployment convenience.
+ *
+ * Same arguments and results as moe_dispatch minus ws/ws_bytes.  Its scratch
+ * is a fixed 1 MiB array inside the library, held by every GPU that loads the
+ * library until the process exits; it fits ceil(T / 256) * n_routed <= 131072
+ * (for example T <= 32768 tokens with 1024 experts, or T <= 131072 with 256).
+ * Larger shapes return MOE_ERR_UNSUPPORTED and launch nothing.  The library
+ * looks up the array's device address on the first call made on each device
+ * (with that device current), so make that first call before any stream
+ * capture.  All calls share the one array, and every call overwrites what it
+ * uses before reading it: calls that may overlap on the GPU (different
+ * streams, or concurrent host threads) race and must be serialised by the
+ * caller.  Allocates nothing. */
+MOE_API moe_status moe_dispatch_static(const moe_shape* shape,
+                                       const int32_t* topk_idx, const void* u,
+                                       int32_t* expert_offsets,
+                                       int32_t* row_token, int32_t* slot_row,
+                                       void* u_perm, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
