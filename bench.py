@@ -18,7 +18,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -40,6 +39,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def load_peaks():
@@ -81,56 +90,69 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and throttle reasons sampled through NVML every 2 ms while the
+    timed region runs (read-only queries; no setting is changed)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, device: torch.device):
+        self.device = device
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = None
+
+    def _handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        p = torch.cuda.get_device_properties(self.device)
+        try:
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+        except Exception:
+            want = str(p.uuid)
+            for i in range(pynvml.nvmlDeviceGetCount()):
+                h = pynvml.nvmlDeviceGetHandleByIndex(i)
+                u = pynvml.nvmlDeviceGetUUID(h)
+                u = u.decode() if isinstance(u, bytes) else u
+                if want in u:
+                    return pynvml, h
+            raise
 
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            nv, h = self._handle()
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        except Exception as e:   # no NVML: report the clocks as unsampled
+            self.error = str(e)
+            return self
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                try:
+                    self.samples.append(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
+                    bits = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    for b, name in self.REASONS.items():
+                        if bits & b:
+                            self.reasons.add(name)
+                except Exception:
+                    pass
+                self._stop.wait(0.002)
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        if self._stop is not None:
+            self._stop.set()
+            self._thread.join()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
 
 class Layer:
@@ -200,7 +222,7 @@ def run_cuda(args):
     ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)]
     barrier()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev) as clk:
         for i in range(K):
             flush.zero_()                       # L2 flushed between timed steps
             starts[i].record()
@@ -209,11 +231,7 @@ def run_cuda(args):
         barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ffn_ms = [a.elapsed_time(b) for a, b in ffn_ev]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dev)
     tokens = shape.T * K * world
     value = tokens / total_s
 
@@ -230,11 +248,7 @@ def run_cuda(args):
         M.moe_layer_forward_host(shape, layer.wt, u_host, h_host, u_dev, layer.h, layer.ws_l)
     e1.record()
     barrier()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
     st, code = M.moe_device_status()
     if st != M.MOE_OK:
         raise RuntimeError(f"device status {st} code {code}")
@@ -321,23 +335,30 @@ def _threads():
         return len(os.sched_getaffinity(0))
 
 
-def cpu_baseline(shape, layer, n_sample):
+def cpu_baseline(shape, layer, n_sample, min_seconds=10.0):
+    """The oracle on bounded samples of the workload's tokens, repeated until
+    about ``min_seconds`` of CPU work; tokens/s over all repetitions."""
     inp = layer.inp
     O, routed_fn, shared_fn, cents, off, bias = _oracle_setup(shape, inp)
-    rows = np.sort(np.random.default_rng(0).choice(shape.T, size=min(n_sample, shape.T),
-                                                   replace=False))
-    u = inp.u[torch.from_numpy(rows).to(inp.u.device)].to(torch.float64).cpu().numpy()
-    # weights of every expert these tokens use are converted before timing
-    z = O.router_logits(u, cents, off)
-    for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
-        routed_fn(int(e))
-    t0 = time.perf_counter()
-    _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
-    dt = time.perf_counter() - t0
-    return {"value": round(len(rows) / dt, 2), "unit": "tokens/s", "cores": _threads(),
-            "kind": "oracle", "sample": f"{len(rows)} of {shape.T} tokens of {shape.name}, "
-            f"full layer (logits, route, dispatch, FFN, combine) in float64 NumPy; "
-            f"weights pre-converted to float64 outside the timing; {dt:.2f} s"}
+    rng = np.random.default_rng(0)
+    n = min(n_sample, shape.T)
+    done, elapsed, reps = 0, 0.0, 0
+    while elapsed < min_seconds and reps < 64:
+        rows = np.sort(rng.choice(shape.T, size=n, replace=False))
+        u = inp.u[torch.from_numpy(rows).to(inp.u.device)].to(torch.float64).cpu().numpy()
+        # weights of every expert these tokens use are converted before timing
+        z = O.router_logits(u, cents, off)
+        for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
+            routed_fn(int(e))
+        t0 = time.perf_counter()
+        _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
+        elapsed += time.perf_counter() - t0
+        done += n
+        reps += 1
+    return {"value": round(done / elapsed, 2), "unit": "tokens/s", "cores": _threads(),
+            "kind": "oracle", "sample": f"{reps} x {n} random tokens of {shape.name} "
+            f"(T={shape.T}): full layer (logits, route, dispatch, FFN, combine) in float64 "
+            f"NumPy, weights pre-converted to float64 outside the timing; {elapsed:.1f} s"}
 
 
 def run_reference(args):
