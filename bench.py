@@ -89,6 +89,60 @@ def recorded_traffic(workload: str):
     return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver; the pynvml wrapper may be absent)."""
+
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._check(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def _check(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} returned {rc}")
+
+    def handle_for_uuid(self, uuid: str):
+        c = self.c
+        n = c.c_uint(0)
+        self._check(self.lib.nvmlDeviceGetCount_v2(c.byref(n)), "nvmlDeviceGetCount_v2")
+        handles = []
+        for i in range(n.value):
+            h = c.c_void_p()
+            self._check(self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(i), c.byref(h)),
+                        "nvmlDeviceGetHandleByIndex_v2")
+            buf = c.create_string_buffer(96)
+            self._check(self.lib.nvmlDeviceGetUUID(h, buf, c.c_uint(96)), "nvmlDeviceGetUUID")
+            if uuid in buf.value.decode():
+                return h
+            handles.append(h)
+        if len(handles) == 1:
+            return handles[0]
+        raise RuntimeError(f"no NVML device with uuid {uuid}")
+
+    def sm_clock(self, h) -> int:
+        v = self.c.c_uint(0)
+        self._check(self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, self.c.byref(v)),
+                    "nvmlDeviceGetClockInfo")
+        return v.value
+
+    def sm_max_clock(self, h) -> int:
+        v = self.c.c_uint(0)
+        self._check(self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, self.c.byref(v)),
+                    "nvmlDeviceGetMaxClockInfo")
+        return v.value
+
+    def event_reasons(self, h) -> int:
+        v = self.c.c_ulonglong(0)
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._check(fn(h, self.c.byref(v)), "nvmlDeviceGetCurrentClocksEventReasons")
+        return v.value
+
+
 class ClockSampler:
     """SM clock and throttle reasons sampled through NVML every 2 ms while the
     timed region runs (read-only queries; no setting is changed)."""
@@ -100,44 +154,29 @@ class ClockSampler:
         self.device = device
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self._stop = None
-
-    def _handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        p = torch.cuda.get_device_properties(self.device)
-        try:
-            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
-            return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-        except Exception:
-            want = str(p.uuid)
-            for i in range(pynvml.nvmlDeviceGetCount()):
-                h = pynvml.nvmlDeviceGetHandleByIndex(i)
-                u = pynvml.nvmlDeviceGetUUID(h)
-                u = u.decode() if isinstance(u, bytes) else u
-                if want in u:
-                    return pynvml, h
-            raise
+        self.error = None
 
     def __enter__(self):
         import threading
         try:
-            nv, h = self._handle()
-            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+            nv = _Nvml()
+            h = nv.handle_for_uuid(str(torch.cuda.get_device_properties(self.device).uuid))
+            self.max_mhz = nv.sm_max_clock(h)
         except Exception as e:   # no NVML: report the clocks as unsampled
-            self.error = str(e)
+            self.error = f"{type(e).__name__}: {e}"
             return self
         self._stop = threading.Event()
 
         def loop():
             while not self._stop.is_set():
                 try:
-                    self.samples.append(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
-                    bits = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    self.samples.append(nv.sm_clock(h))
+                    bits = nv.event_reasons(h)
                     for b, name in self.REASONS.items():
                         if bits & b:
                             self.reasons.add(name)
-                except Exception:
-                    pass
+                except Exception as e:
+                    self.error = f"{type(e).__name__}: {e}"
                 self._stop.wait(0.002)
         self._thread = threading.Thread(target=loop, daemon=True)
         self._thread.start()
@@ -150,7 +189,8 @@ class ClockSampler:
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "error": self.error}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 

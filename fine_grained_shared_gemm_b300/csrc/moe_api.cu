@@ -7,7 +7,9 @@
 #include <cuda_runtime.h>
 #include <string.h>
 
+#include <algorithm>
 #include <climits>
+#include <cmath>
 #include <mutex>
 
 #include "moe.h"
@@ -121,25 +123,54 @@ moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, u
   return MOE_OK;
 }
 
-template <int EPI, int BN>
-moe_status launch_tc(const tc::Params& p, int grid, cudaStream_t st) {
-  using C = tc::Config<BN>;
-  static bool configured[64] = {false};
+// Launches the grouped GEMM persistently: one CTA per SM, or for PAIR == 2
+// as many two-CTA clusters as fit on the device at once (at most max_ctas
+// CTAs).  The dynamic shared-memory limit and the grid are set up once per
+// device.
+template <int EPI, int BN, int PAIR>
+moe_status launch_tc(const tc::Params& p, int max_ctas, cudaStream_t st) {
+  using C = tc::Config<BN, PAIR>;
+  auto kern = tc::grouped_gemm_kernel<EPI, BN, PAIR>;
+  static int grid_for[64] = {0};
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    MOE_CUDA(cudaFuncSetAttribute(tc::grouped_gemm_kernel<EPI, BN>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(tc::kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR == 2 ? 1 : 0;
+  if (grid_for[dev] == 0) {
+    MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  C::kSmemBytes));
+    int g = num_sms();
+    if (PAIR == 2) {
+      int clusters = 0;
+      cfg.gridDim = dim3(static_cast<unsigned>(g - g % 2), 1, 1);
+      MOE_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
+      if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+      g = 2 * clusters;
+    }
+    grid_for[dev] = g;
   }
-  tc::grouped_gemm_kernel<EPI, BN><<<grid, tc::kNumThreads, C::kSmemBytes, st>>>(p);
-  MOE_CUDA(cudaGetLastError());
+  int grid = std::min(grid_for[dev], std::max(max_ctas, PAIR));
+  grid -= grid % PAIR;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  MOE_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
   return MOE_OK;
 }
 
+// Expert GEMMs: 256-token tiles on CTA pairs, 64-token tiles on single CTAs.
 template <int EPI>
-moe_status launch_tc_bn(const tc::Params& p, int bn, int grid, cudaStream_t st) {
-  return bn == 256 ? launch_tc<EPI, 256>(p, grid, st) : launch_tc<EPI, 64>(p, grid, st);
+moe_status launch_ffn(const tc::Params& p, int bn, cudaStream_t st) {
+  return bn == 256 ? launch_tc<EPI, 256, 2>(p, INT_MAX, st) : launch_tc<EPI, 64, 1>(p, INT_MAX, st);
 }
 
 // ---------------------------------------------------------------- workspace
@@ -274,7 +305,8 @@ moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
   p.col_offset = off;
   const int bn = (T > 64 && p.n_wtiles * cdiv(T, 256) >= num_sms()) ? 256 : 64;
   const int tiles = p.n_wtiles * cdiv(T, bn);
-  return launch_tc_bn<tc::EPI_F32>(p, bn, std::min(tiles, num_sms()), st);
+  return bn == 256 ? launch_tc<tc::EPI_F32, 256, 1>(p, tiles, st)
+                   : launch_tc<tc::EPI_F32, 64, 1>(p, tiles, st);
 }
 
 moe_status do_route(const moe_shape* s, const float* logits, const float* bias, int32_t* idx,
@@ -400,16 +432,18 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   MOE_TRY(make_token_maps(p.b[1], u, T, H));
   if (Tk) MOE_TRY(make_token_maps(p.b[0], u_perm, Tk, H));
   else memcpy(p.b[0], p.b[1], sizeof(p.b[0]));
+  // wide token tiles run on CTA pairs: 256 weight rows per tile
+  const int pair = bn == 256 ? 2 : 1;
   p.groups = f.g1;
   p.tile_prefix = f.tile_prefix;
   p.n_groups = G;
-  p.n_wtiles = I / static_cast<int>(a1_box);
+  p.n_wtiles = cdiv(I, static_cast<int>(a1_box) * pair);
   p.num_k_blocks = cdiv(H, tc::kBK);
   p.out[0] = p.out[1] = f.act;
   p.out_ld = I;
   p.out_cols = I;
-  if (swiglu) MOE_TRY(launch_tc_bn<tc::EPI_SWIGLU>(p, bn, num_sms(), st));
-  else MOE_TRY(launch_tc_bn<tc::EPI_RELU>(p, bn, num_sms(), st));
+  if (swiglu) MOE_TRY(launch_ffn<tc::EPI_SWIGLU>(p, bn, st));
+  else MOE_TRY(launch_ffn<tc::EPI_RELU>(p, bn, st));
 
   // ---- GEMM2: down projection
   tc::Params q;
@@ -424,13 +458,13 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   q.groups = f.g2;
   q.tile_prefix = f.tile_prefix;
   q.n_groups = G;
-  q.n_wtiles = H / tc::kBM;
+  q.n_wtiles = cdiv(H, tc::kBM * pair);
   q.num_k_blocks = cdiv(I, tc::kBK);
   q.out[0] = Tk ? y_perm : y_shared;
   q.out[1] = Ks ? y_shared : y_perm;
   q.out_ld = H;
   q.out_cols = H;
-  return launch_tc_bn<tc::EPI_BF16>(q, bn, num_sms(), st);
+  return launch_ffn<tc::EPI_BF16>(q, bn, st);
 }
 
 moe_status do_combine(const moe_shape* s, const void* u, const void* y_perm,

@@ -1,11 +1,12 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
 // for the expert FFNs and the router logits of the MoE layer.
 //
-// Orientation ("swap-AB"): the weight rows are the MMA's M side (128 rows per
-// tile) and the token rows are its N side.  The ragged number of tokens each
-// expert receives then only sets N, which the tensor core takes in steps of
-// 16, so a partly filled expert costs little extra work; decode-sized groups
-// of one or two tokens run at N = 16 while the weights stream at full width.
+// Orientation ("swap-AB"): the weight rows are the MMA's M side and the token
+// rows are its N side.  The ragged number of tokens each expert receives then
+// only sets N, which the tensor core takes in steps of 16 (32 for a CTA
+// pair), so a partly filled expert costs little extra work; decode-sized
+// groups of one or two tokens run at N = 16 while the weights stream at full
+// width.
 //
 //   D[j, c] = Σ_k W[j, k] · X[c, k]      (j: weight row, c: token of the group)
 //
@@ -14,11 +15,30 @@
 // swizzle, and the fp32 accumulator lives in tensor memory (TMEM), double
 // buffered so the epilogue of one tile overlaps the MMAs of the next.
 //
+// PAIR = 1: one CTA per tile of 128 weight rows x up to BN tokens.
+// PAIR = 2: a cluster of two CTAs on two SMs shares one tile of 256 weight
+//   rows x up to BN tokens through tcgen05.mma.cta_group::2.  Each CTA loads
+//   its own 128 weight rows and HALF of the token rows; the tensor cores of
+//   the pair exchange the token halves, so each SM pulls 16 KB of tokens per
+//   k-block instead of 32 KB and the pipeline holds six stages instead of
+//   four.  Each CTA's TMEM receives its own 128 rows of D.  The CTA of rank 0
+//   (the leader) issues the MMAs; both CTAs' copies complete on the leader's
+//   "full" barriers, and the leader's commits arrive on both CTAs' barriers.
+//
 // Roles (192 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one thread)
-//   warp 1      TMEM allocation and MMA issue (one thread)
+//   warp 1      TMEM allocation and (leader only) MMA issue (one thread)
 //   warps 2..5  epilogue: TMEM -> registers -> shared-memory transpose ->
 //               global, with the FFN activation fused in
+//
+// The producer hands the MMA thread each stage's instruction descriptor
+// through shared memory, so the MMA thread never decodes tiles; the per-group
+// tile prefix is staged in shared memory for the decoders.
+//
+// Token tiles are balanced: a group of `count` rows is cut into
+// ceil(count / BN) tiles of equal height (rounded up to the MMA step), and
+// each tile loads exactly the rows its MMA reads, as a sum of power-of-two TMA
+// boxes.
 //
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel sets a bit of the
 // device error word, lets every role leave its loop, waits for its own copies
@@ -33,12 +53,13 @@ namespace moe {
 namespace tc {
 
 constexpr int kBK = 64;            // contraction elements per stage: one 128-byte swizzle row
-constexpr int kBM = 128;           // MMA M (weight rows per tile)
+constexpr int kBM = 128;           // weight rows per CTA per tile (MMA M per CTA)
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma for 16-bit inputs
 constexpr int kNumThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
 constexpr int kStageBufFloats = 4 * 32 * 33;
+constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 family
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
 
@@ -48,34 +69,73 @@ struct Params {
   CUtensorMap b[2][kNumBoxes];   // token sources x box heights
   const GroupDesc* groups;       // [n_groups], or null for one dense group
   const int* tile_prefix;        // [n_groups + 1] prefix sum of token tiles
-  int n_groups;
+  int n_groups;                  // <= kMaxGroups
   int dense_count;               // token rows of the dense group
-  int n_wtiles;                  // weight tiles per group
+  int n_wtiles;                  // weight tiles (of 128 * PAIR rows) per group
   int num_k_blocks;              // ceil(K / kBK)
   void* out[2];
   int out_ld;                    // output row pitch in elements
-  int out_cols;                  // valid output columns (EPI_F32)
+  int out_cols;                  // valid output columns
   const float* col_offset;       // EPI_F32: per-column addend, may be null
 };
 
-template <int BN>
+constexpr int kMaxGroups = 1024;
+
+template <int BN, int PAIR>
 struct Config {
-  static constexpr int kBBytes = BN * kBK * 2;
+  static_assert(PAIR == 1 || PAIR == 2, "a tile is shared by one or two CTAs");
+  static constexpr int kBRows = BN / PAIR;              // token rows one CTA holds
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (196608 / kStageBytes) > 12 ? 12 : (196608 / kStageBytes);
-  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
+  static constexpr int kPrefixBytes = (kMaxGroups + 4) * 4;
+  static constexpr int kEpiBytes = kStageBufFloats * 4;
+  static constexpr int kFit =
+      (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
+  static constexpr int kStages = kFit > 16 ? 16 : kFit;
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kBarBytes + kStageBufFloats * 4;
+      1024 + kStages * kStageBytes + kBarBytes + kPrefixBytes + kEpiBytes;
+  static constexpr int kStep = 16 * PAIR;               // MMA N granularity
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // double-buffered accumulator
   static_assert(kStages >= 2, "pipeline too shallow");
-  static_assert(2 * kStages + 5 <= kBarBytes / 8 - 1, "barrier area too small");
-  static_assert(kSmemBytes <= 232448, "shared memory over the sm_100-family limit");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory over the sm_100-family limit");
+  static_assert(BN % kStep == 0 && kBRows <= 256, "token tile");
 };
 
 // ------------------------------------------------------------------ PTX
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in the CTA of the given rank.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -96,37 +156,65 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive on a barrier given by its shared::cluster address (own CTA or peer).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+template <bool kClusterScope>
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kClusterScope)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok;
 }
 
 // Waits for the phase of the given parity to complete; false after the limit.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 
+// 2-D tiled TMA load into this CTA's shared memory.  With PAIR == 2 the
+// completion is signalled on `bar`, a shared::cluster address that may be the
+// peer CTA's barrier.
+template <int PAIR>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
+  if (PAIR == 1)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -140,16 +228,33 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// TMEM allocation: with PAIR == 2 one warp of each CTA of the pair issues it
+// and both receive the same columns.
+template <int PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if (PAIR == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
 }
 
+template <int PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if (PAIR == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -163,23 +268,56 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+// m is the MMA's full M (256 for a CTA pair).
 __device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+template <int PAIR>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (PAIR == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+// Arrive (once) on `bar` when all MMAs issued so far by this thread complete.
+// PAIR == 2: on the barrier at the same offset in both CTAs of the pair.
+template <int PAIR>
+__device__ __forceinline__ void tc_commit_all(uint32_t bar) {
+  if (PAIR == 1) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  } else {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+  }
+}
+
+// Arrive on this CTA's `bar` only.
+template <int PAIR>
+__device__ __forceinline__ void tc_commit_local(uint32_t bar) {
+  if (PAIR == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
 }
 
 // 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
@@ -226,19 +364,21 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
 
 // ------------------------------------------------------------------ tiles
 
+// One tile as seen by one CTA (of rank `rank` in its pair).
 struct Tile {
-  int a_sel, a_row, a3_row;
-  int b_src, b_row;
-  int out_sel, out_row, out_col;
-  int n_valid;
+  int a_sel, a_row;      // weight stack and this CTA's first weight row
+  int b_src, b_row;      // token source and this CTA's first token row
+  int b_rows;            // token rows this CTA loads (multiple of 16)
+  int n_mma;             // MMA N: token rows of the whole tile, rounded up
+  int out_sel, out_row;  // output buffer and the tile's first output row
+  int out_col;           // this CTA's first output column
+  int n_valid;           // valid token rows of the tile
 };
 
-__device__ __forceinline__ int box_index(int n) {
-  return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : n <= 128 ? 3 : 4;
-}
-
-template <int EPI, int BN>
-__device__ __forceinline__ Tile decode_tile(const Params& p, int t) {
+// prefix: the tile prefix staged in shared memory (unused for a dense group).
+template <int EPI, int BN, int PAIR>
+__device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, int t, int rank) {
+  constexpr int kStep = Config<BN, PAIR>::kStep;
   const int nw = p.n_wtiles;
   GroupDesc d;
   int nt, local;
@@ -250,34 +390,36 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int t) {
     int lo = 0, hi = p.n_groups;  // largest g with prefix[g] * nw <= t
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(p.tile_prefix + mid) * nw <= t) lo = mid; else hi = mid;
+      if (prefix[mid] * nw <= t) lo = mid; else hi = mid;
     }
     d = p.groups[lo];
-    const int pre = __ldg(p.tile_prefix + lo);
-    nt = __ldg(p.tile_prefix + lo + 1) - pre;
-    local = t - pre * nw;
+    nt = prefix[lo + 1] - prefix[lo];
+    local = t - prefix[lo] * nw;
   }
   const int w = local / nt, n = local - w * nt;
+  // nt = ceil(count / BN) tiles of equal height th <= BN; the last is never empty
+  const int th = ((d.count + nt - 1) / nt + kStep - 1) / kStep * kStep;
+  constexpr int kCols = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;  // output columns per CTA
   Tile tl;
-  constexpr int kRowsPerW = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;
   tl.a_sel = d.a_sel;
-  tl.a_row = d.a_row0 + w * kRowsPerW;
-  tl.a3_row = tl.a_row;
+  tl.a_row = d.a_row0 + (w * PAIR + rank) * kCols;
+  tl.n_valid = min(th, d.count - n * th);
+  tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
+  tl.b_rows = tl.n_mma / PAIR;
   tl.b_src = d.b_src;
-  tl.b_row = d.b_row0 + n * BN;
+  tl.b_row = d.b_row0 + n * th + rank * tl.b_rows;
   tl.out_sel = d.out_sel;
-  tl.out_row = d.out_row0 + n * BN;
-  tl.out_col = w * kRowsPerW;
-  tl.n_valid = min(BN, d.count - n * BN);
+  tl.out_row = d.out_row0 + n * th;
+  tl.out_col = (w * PAIR + rank) * kCols;
   return tl;
 }
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI, int BN>
+template <int EPI, int BN, int PAIR>
 __global__ void __launch_bounds__(kNumThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ Params p) {
-  using C = Config<BN>;
+  using C = Config<BN, PAIR>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -285,14 +427,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t bar0 = base + S * C::kStageBytes;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
-  const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
-  float* stage_buf = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
+  auto empty_bar = [&](int s) { return bar0 + 128u + 8u * s; };
+  auto tfull_bar = [&](int a) { return bar0 + 256u + 8u * a; };
+  auto tempty_bar = [&](int a) { return bar0 + 272u + 8u * a; };
+  const uint32_t done_bar = bar0 + 288u;
+  uint8_t* bar_area = smem + S * C::kStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 296);
+  volatile uint32_t* idesc_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 320);
+  int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
+  float* stage_buf = reinterpret_cast<float*>(bar_area + C::kBarBytes + C::kPrefixBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR == 2 ? cluster_rank() : 0u;
+  const int first = PAIR == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int stride = PAIR == 2 ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -301,7 +449,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), 4 * PAIR);  // lane 0 of each epilogue warp of each CTA
     }
     mbar_init(done_bar, 1);
     fence_barrier_init();
@@ -312,14 +460,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (EPI == EPI_SWIGLU) prefetch_map(&p.a3[i]);
     }
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  if (p.groups != nullptr)
+    for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) s_prefix[i] = __ldg(p.tile_prefix + i);
+  if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // the peer's barriers are initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int tiles_per_w = (p.groups == nullptr) ? (p.dense_count + BN - 1) / BN
-                                                : __ldg(p.tile_prefix + p.n_groups);
+                                                : s_prefix[p.n_groups];
   const int total = p.n_wtiles * tiles_per_w;
   const int nk = p.num_k_blocks;
 
@@ -329,11 +480,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<EPI, BN>(p, t);
-        const int box = box_index(tl.n_valid);
-        const uint32_t bytes = kABytes + (16u << box) * (kBK * 2);
-        const CUtensorMap* bmap = &p.b[tl.b_src][box];
+      for (int t = first; t < total && ok; t += stride) {
+        const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
+        // bytes both CTAs' copies deliver to the leader's barrier
+        const uint32_t bytes = PAIR * kABytes + static_cast<uint32_t>(tl.n_mma) * (kBK * 2);
+        const uint32_t idesc = idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma));
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
@@ -341,37 +492,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             break;
           }
           const uint32_t sa = base + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
-          armed |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sa, &p.a[tl.a_sel], full_bar(stage), kb * kBK, tl.a_row);
-            tma_load_2d(sa + kABytes / 2, &p.a3[tl.a_sel], full_bar(stage), kb * kBK, tl.a3_row);
-          } else {
-            tma_load_2d(sa, &p.a[tl.a_sel], full_bar(stage), kb * kBK, tl.a_row);
+          uint32_t fb = full_bar(stage);
+          if (rank == 0) {
+            idesc_slot[stage] = idesc;
+            mbar_arrive_expect_tx(fb, bytes);
+            armed |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d(sa + kABytes, bmap, full_bar(stage), kb * kBK, tl.b_row);
+          if (PAIR == 2) fb = map_to_rank(fb, 0);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d<PAIR>(sa, &p.a[tl.a_sel], fb, kb * kBK, tl.a_row);
+            tma_load_2d<PAIR>(sa + kABytes / 2, &p.a3[tl.a_sel], fb, kb * kBK, tl.a_row);
+          } else {
+            tma_load_2d<PAIR>(sa, &p.a[tl.a_sel], fb, kb * kBK, tl.a_row);
+          }
+          // this CTA's token rows as boxes of 256/128/64/32/16 rows
+          int off = 0;
+#pragma unroll
+          for (int i = kNumBoxes - 1; i >= 0; --i) {
+            const int rows = 16 << i;
+            if (rows <= C::kBRows && (tl.b_rows & rows)) {
+              tma_load_2d<PAIR>(sa + kABytes + off * (kBK * 2), &p.b[tl.b_src][i], fb, kb * kBK,
+                                tl.b_row + off);
+              off += rows;
+            }
+          }
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
-      // No copy may land after the CTA exits: wait for the last one per stage.
-      for (int s = 0; s < S; ++s)
-        if ((armed >> s) & 1u)
-          if (!mbar_wait(full_bar(s), (last_parity >> s) & 1u))
-            raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
+      // No copy may land after the CTA exits: the leader waits for the last
+      // armed phase of every stage (which also covers the peer's copies).
+      if (rank == 0)
+        for (int s = 0; s < S; ++s)
+          if ((armed >> s) & 1u)
+            if (!mbar_wait(full_bar(s), (last_parity >> s) & 1u))
+              raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<EPI, BN>(p, t);
-        const uint32_t n_mma = (static_cast<uint32_t>(tl.n_valid) + 15u) & ~15u;
-        const uint32_t idesc = idesc_bf16(kBM, n_mma);
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1)) {
+      for (int t = first; t < total && ok; t += stride) {
+        if (!mbar_wait<PAIR == 2>(tempty_bar(acc), acc_phase ^ 1)) {
           raise_device_error(DEV_ERR_TIMEOUT_MMA);
           break;
         }
@@ -384,21 +549,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint32_t idesc = idesc_slot[stage];
           const uint32_t sa = base + stage * C::kStageBytes;
           const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + kABytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            tc_mma(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-          tc_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+            tc_mma<PAIR>(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          tc_commit_all<PAIR>(empty_bar(stage));  // frees the stage in both CTAs once read
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));
+        tc_commit_all<PAIR>(tfull_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       // All MMAs issued by this thread complete before TMEM is freed.
-      tc_commit(done_bar);
+      tc_commit_local<PAIR>(done_bar);
       if (!mbar_wait(done_bar, 0)) raise_device_error(DEV_ERR_TIMEOUT_MMA);
     }
     __syncwarp();
@@ -406,10 +572,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quarter this warp may read
     float* buf = stage_buf + q * 32 * 33;
+    // the leader's accumulator-free barriers, as shared::cluster addresses
+    const uint32_t tempty_leader0 = PAIR == 2 ? map_to_rank(tempty_bar(0), 0) : tempty_bar(0);
+    const uint32_t tempty_leader1 = PAIR == 2 ? map_to_rank(tempty_bar(1), 0) : tempty_bar(1);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<EPI, BN>(p, t);
+    for (int t = first; t < total; t += stride) {
+      const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
       const bool ready = mbar_wait(tfull_bar(acc), acc_phase);
       // all four epilogue warps leave together, so no named barrier is left half-arrived
       if (!named_bar_and(1, 128, ready)) {
@@ -417,12 +586,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         break;
       }
       tc_fence_after();
+      const bool cols_ok = tl.out_col < p.out_cols;  // a CTA half past the last row stores nothing
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) +
                             (static_cast<uint32_t>(q * 32) << 16);
       for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tacc + c0, v);
-        const bool row_ok = c0 + lane < tl.n_valid;
+        const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
         const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
         if (EPI == EPI_SWIGLU) {
           // lanes 0..63 hold the gate rows, 64..127 the matching up rows
@@ -490,8 +660,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           __syncwarp();
         }
       }
+      // this warp has read the accumulator: tell the leader's MMA issuer
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR == 2) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+        else mbar_arrive(tempty_bar(acc));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -499,8 +674,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // neither CTA leaves while the pair may still touch it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) tmem_dealloc<PAIR>(tmem_base, C::kTmemCols);
 }
 
 }  // namespace tc

@@ -116,6 +116,20 @@ SHAPES = {
             dtype="bf16", bias_range=0.1,
             description="DeepSeek-V3-shaped prefill layer: 1 shared + 256 routed "
                         "SwiGLU experts of width 2048, top-8 sigmoid + bias"),
+        # Smaller layers with the same per-expert GEMM shapes as two of the
+        # layers above (same H, width and rows per expert, fewer experts), for
+        # hardware-counter captures that must stay a few GB on the device.
+        MoEShape(
+            name="v3_prefill_e32_bf16", T=1024, H=7168, n_routed=32, n_shared=1,
+            top_k=8, inter=2048, gate=GATE_SIGMOID_BIAS, act=ACT_SWIGLU,
+            dtype="bf16", bias_range=0.1,
+            description="V3-shaped prefill layer cut to 32 routed experts and 1024 "
+                        "tokens: 256 rows per expert as in the full layer"),
+        MoEShape(
+            name="sweep_m16_e32_bf16", T=16384, H=2048, n_routed=32, n_shared=0,
+            top_k=4, inter=256, gate=GATE_SOFTMAX, act=ACT_SWIGLU, dtype="bf16",
+            description="granularity m=16 expert shape (width 256, 2048 rows per "
+                        "expert) with 32 experts"),
         MoEShape(
             name="decode_bf16", T=64, H=7168, n_routed=384, n_shared=1, top_k=8,
             inter=2048, gate=GATE_SIGMOID_BIAS, act=ACT_SWIGLU, dtype="bf16",

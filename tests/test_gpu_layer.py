@@ -116,7 +116,8 @@ def test_layer_host_buffers_match_device_path():
 
 
 # full-size page-shaped layers: (shape name, sampled tokens)
-FULL = [("dsmoe16b_bf16", 48), ("v3_prefill_bf16", 12), ("decode_bf16", 8)] + \
+FULL = [("dsmoe16b_bf16", 48), ("v3_prefill_bf16", 12), ("decode_bf16", 8),
+        ("v3_prefill_e32_bf16", 16), ("sweep_m16_e32_bf16", 24)] + \
     [(f"sweep_m{m}{v}", 24) for v in ("", "_shared1") for m in (1, 2, 4, 8, 16)]
 
 
