@@ -101,25 +101,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [rows, cols] row-major, box of 64 columns (128 bytes) x box_rows rows,
-// 128-byte swizzle, zero fill outside the tensor.
-moe_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows) {
+moe_status encode(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cuda_fail(cudaErrorNotSupported);
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::kBK), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
+// bf16 [rows, cols] row-major (cols % 64 == 0) viewed as (64 columns, rows,
+// cols / 64 chunks): a box of box_rows rows x tc::kKPS chunks lands the
+// chunks one after the other, each box_rows x 128 bytes, 128-byte swizzled.
+// Chunks past the end are zero-filled.
+moe_status make_map3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::kBK), rows, cols / tc::kBK};
+  const cuuint64_t strides[2] = {cols * 2, tc::kBK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(tc::kBK), box_rows, tc::kKPS};
+  return encode(m, 3, base, dims, strides, box);
+}
+
+// SwiGLU gate and up stacks w1, w3 (both bf16 [rows, cols], rows % 64 == 0)
+// as one 5-D tensor (64 columns, 64 rows, {first, second} stack, 64-row
+// blocks, cols / 64 chunks) whose third dimension steps between the two
+// allocations.  One box lands, for each of tc::kKPS chunks, 64 rows of the
+// lower-addressed stack then the same 64 rows of the other: *up_first says
+// whether that is W3.  The two allocations must be less than 2^40 bytes apart.
+moe_status make_map5_gate_up(CUtensorMap* m, const void* w1, const void* w3, uint64_t rows,
+                             uint64_t cols, int* up_first) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w1), b = reinterpret_cast<uintptr_t>(w3);
+  *up_first = b < a;
+  const uintptr_t gap = b < a ? a - b : b - a;
+  if (gap == 0 || gap >= (static_cast<uintptr_t>(1) << 40)) return MOE_ERR_UNSUPPORTED;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(tc::kBK), 64, 2, rows / 64, cols / tc::kBK};
+  const cuuint64_t strides[4] = {cols * 2, static_cast<cuuint64_t>(gap), 64 * cols * 2,
+                                 tc::kBK * 2};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(tc::kBK), 64, 2, 1, tc::kKPS};
+  return encode(m, 5, b < a ? w3 : w1, dims, strides, box);
+}
+
 // Token-source maps for every box height.
 moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, uint64_t cols) {
-  for (int i = 0; i < tc::kNumBoxes; ++i) MOE_TRY(make_map(&maps[i], base, rows, cols, 16u << i));
+  for (int i = 0; i < tc::kNumBoxes; ++i) MOE_TRY(make_map3(&maps[i], base, rows, cols, 16u << i));
   return MOE_OK;
 }
 
@@ -289,9 +315,8 @@ moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
   }
   tc::Params p;
   memset(&p, 0, sizeof(p));
-  MOE_TRY(make_map(&p.a[0], cent, E, H, tc::kBM));
+  MOE_TRY(make_map3(&p.a[0], cent, E, H, tc::kBM));
   p.a[1] = p.a[0];
-  p.a3[0] = p.a3[1] = p.a[0];
   MOE_TRY(make_token_maps(p.b[0], u, T, H));
   memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
   p.groups = nullptr;
@@ -417,17 +442,21 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   // ---- GEMM1: gate/up projection with the activation fused in the epilogue
   tc::Params p;
   memset(&p, 0, sizeof(p));
-  const uint32_t a1_box = swiglu ? tc::kBM / 2 : tc::kBM;
-  MOE_TRY(make_map(&p.a[0], wt->w1, static_cast<uint64_t>(E) * I, H, a1_box));
-  if (Ks) MOE_TRY(make_map(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H, a1_box));
-  else p.a[1] = p.a[0];
+  const uint32_t a1_box = swiglu ? tc::kBM / 2 : tc::kBM;  // output columns per CTA
   if (swiglu) {
-    MOE_TRY(make_map(&p.a3[0], wt->w3, static_cast<uint64_t>(E) * I, H, a1_box));
-    if (Ks) MOE_TRY(make_map(&p.a3[1], wt->sw3, static_cast<uint64_t>(Ks) * I, H, a1_box));
-    else p.a3[1] = p.a3[0];
+    MOE_TRY(make_map5_gate_up(&p.a[0], wt->w1, wt->w3, static_cast<uint64_t>(E) * I, H,
+                              &p.up_first[0]));
+    if (Ks)
+      MOE_TRY(make_map5_gate_up(&p.a[1], wt->sw1, wt->sw3, static_cast<uint64_t>(Ks) * I, H,
+                                &p.up_first[1]));
+    else {
+      p.a[1] = p.a[0];
+      p.up_first[1] = p.up_first[0];
+    }
   } else {
-    p.a3[0] = p.a[0];
-    p.a3[1] = p.a[1];
+    MOE_TRY(make_map3(&p.a[0], wt->w1, static_cast<uint64_t>(E) * I, H, tc::kBM));
+    if (Ks) MOE_TRY(make_map3(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H, tc::kBM));
+    else p.a[1] = p.a[0];
   }
   MOE_TRY(make_token_maps(p.b[1], u, T, H));
   if (Tk) MOE_TRY(make_token_maps(p.b[0], u_perm, Tk, H));
@@ -448,11 +477,9 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   // ---- GEMM2: down projection
   tc::Params q;
   memset(&q, 0, sizeof(q));
-  MOE_TRY(make_map(&q.a[0], wt->w2, static_cast<uint64_t>(E) * H, I, tc::kBM));
-  if (Ks) MOE_TRY(make_map(&q.a[1], wt->sw2, static_cast<uint64_t>(Ks) * H, I, tc::kBM));
+  MOE_TRY(make_map3(&q.a[0], wt->w2, static_cast<uint64_t>(E) * H, I, tc::kBM));
+  if (Ks) MOE_TRY(make_map3(&q.a[1], wt->sw2, static_cast<uint64_t>(Ks) * H, I, tc::kBM));
   else q.a[1] = q.a[0];
-  q.a3[0] = q.a[0];
-  q.a3[1] = q.a[1];
   MOE_TRY(make_token_maps(q.b[0], f.act, rows_act, I));
   memcpy(q.b[1], q.b[0], sizeof(q.b[0]));
   q.groups = f.g2;

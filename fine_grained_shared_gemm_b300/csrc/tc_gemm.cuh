@@ -35,10 +35,21 @@
 // through shared memory, so the MMA thread never decodes tiles; the per-group
 // tile prefix is staged in shared memory for the decoders.
 //
-// Token tiles are balanced: a group of `count` rows is cut into
-// ceil(count / BN) tiles of equal height (rounded up to the MMA step), and
-// each tile loads exactly the rows its MMA reads, as a sum of power-of-two TMA
-// boxes.
+// A pipeline stage holds two k-blocks (K = 128) and is filled by exactly two
+// TMA copies: one for the weight tile and one for the token tile.  Each SM
+// takes in at most ~50 bytes per clock through TMA, and a copy carries a fixed
+// cost on top of its bytes, so few, large copies are what keep the tensor
+// core fed.  The copies use tensor maps with a k-chunk dimension (stride
+// 128 bytes) so that one box lands both k-blocks, one after the other, each
+// in the 128-byte-swizzled K-major layout the MMA reads:
+//   weights  3-D map (64 columns, rows, K/64 chunks), box 64 x 128 x 2;
+//   SwiGLU   5-D map (64 columns, 64 rows, {W1, W3}, 64-row blocks, chunks)
+//            whose third dimension steps from W1 to W3 (stride w3 - w1), so
+//            one box lands [64 gate rows; 64 up rows] for both k-blocks;
+//   tokens   3-D map, box 64 x R x 2 with R the next power of two >= the
+//            rows the tile's MMA reads (extra rows are loaded, never used).
+// A group's tokens are cut into full tiles of BN rows and one tail tile.  A
+// chunk past the end of K is zero-filled by TMA and adds nothing.
 //
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel sets a bit of the
 // device error word, lets every role leave its loop, waits for its own copies
@@ -52,7 +63,8 @@
 namespace moe {
 namespace tc {
 
-constexpr int kBK = 64;            // contraction elements per stage: one 128-byte swizzle row
+constexpr int kBK = 64;            // contraction elements per k-block: one 128-byte swizzle row
+constexpr int kKPS = 2;            // k-blocks per pipeline stage
 constexpr int kBM = 128;           // weight rows per CTA per tile (MMA M per CTA)
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma for 16-bit inputs
 constexpr int kNumThreads = 192;
@@ -64,9 +76,8 @@ constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 fa
 enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
 
 struct Params {
-  CUtensorMap a[2];              // weight stacks (routed, shared)
-  CUtensorMap a3[2];             // SwiGLU up-projection stacks
-  CUtensorMap b[2][kNumBoxes];   // token sources x box heights
+  CUtensorMap a[2];              // weight stacks (routed, shared): 3-D, or 5-D for SwiGLU
+  CUtensorMap b[2][kNumBoxes];   // token sources x box heights: 3-D
   const GroupDesc* groups;       // [n_groups], or null for one dense group
   const int* tile_prefix;        // [n_groups + 1] prefix sum of token tiles
   int n_groups;                  // <= kMaxGroups
@@ -77,6 +88,7 @@ struct Params {
   int out_ld;                    // output row pitch in elements
   int out_cols;                  // valid output columns
   const float* col_offset;       // EPI_F32: per-column addend, may be null
+  int up_first[2];               // SwiGLU, per stack: the 5-D map lands the up rows first
 };
 
 constexpr int kMaxGroups = 1024;
@@ -85,14 +97,14 @@ template <int BN, int PAIR>
 struct Config {
   static_assert(PAIR == 1 || PAIR == 2, "a tile is shared by one or two CTAs");
   static constexpr int kBRows = BN / PAIR;              // token rows one CTA holds
-  static constexpr int kBBytes = kBRows * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBBytes = kBRows * kBK * 2;      // one k-block of tokens
+  static constexpr int kStageBytes = kKPS * (kABytes + kBBytes);
   static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
   static constexpr int kPrefixBytes = (kMaxGroups + 4) * 4;
   static constexpr int kEpiBytes = kStageBufFloats * 4;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
-  static constexpr int kStages = kFit > 16 ? 16 : kFit;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + kBarBytes + kPrefixBytes + kEpiBytes;
   static constexpr int kStep = 16 * PAIR;               // MMA N granularity
@@ -197,23 +209,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// 2-D tiled TMA load into this CTA's shared memory.  With PAIR == 2 the
+// Tiled TMA loads into this CTA's shared memory.  With PAIR == 2 the
 // completion is signalled on `bar`, a shared::cluster address that may be the
 // peer CTA's barrier.
 template <int PAIR>
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
   if (PAIR == 1)
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
   else
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+template <int PAIR>
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  if (PAIR == 1)
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(c4)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(c4)
         : "memory");
 }
 
@@ -364,11 +395,16 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
 
 // ------------------------------------------------------------------ tiles
 
+__device__ __forceinline__ int box_index(int rows) {
+  return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : rows <= 128 ? 3 : 4;
+}
+
 // One tile as seen by one CTA (of rank `rank` in its pair).
 struct Tile {
   int a_sel, a_row;      // weight stack and this CTA's first weight row
   int b_src, b_row;      // token source and this CTA's first token row
-  int b_rows;            // token rows this CTA loads (multiple of 16)
+  int b_rows;            // token rows this CTA's half of the MMA reads (multiple of 16)
+  int b_box;             // box index: the copy lands 16 << b_box >= b_rows rows
   int n_mma;             // MMA N: token rows of the whole tile, rounded up
   int out_sel, out_row;  // output buffer and the tile's first output row
   int out_col;           // this CTA's first output column
@@ -397,8 +433,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
     local = t - prefix[lo] * nw;
   }
   const int w = local / nt, n = local - w * nt;
-  // nt = ceil(count / BN) tiles of equal height th <= BN; the last is never empty
-  const int th = ((d.count + nt - 1) / nt + kStep - 1) / kStep * kStep;
+  const int th = BN;  // full tiles of BN rows, then the tail
   constexpr int kCols = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;  // output columns per CTA
   Tile tl;
   tl.a_sel = d.a_sel;
@@ -406,6 +441,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.n_valid = min(th, d.count - n * th);
   tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
   tl.b_rows = tl.n_mma / PAIR;
+  tl.b_box = box_index(tl.b_rows);
   tl.b_src = d.b_src;
   tl.b_row = d.b_row0 + n * th + rank * tl.b_rows;
   tl.out_sel = d.out_sel;
@@ -434,6 +470,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint8_t* bar_area = smem + S * C::kStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 296);
   volatile uint32_t* idesc_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 320);
+  volatile uint32_t* boff_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 384);
   int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
   float* stage_buf = reinterpret_cast<float*>(bar_area + C::kBarBytes + C::kPrefixBytes);
 
@@ -457,7 +494,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < 2; ++i) {
       prefetch_map(&p.a[i]);
-      if (EPI == EPI_SWIGLU) prefetch_map(&p.a3[i]);
     }
   }
   if (p.groups != nullptr)
@@ -482,10 +518,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int t = first; t < total && ok; t += stride) {
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
-        // bytes both CTAs' copies deliver to the leader's barrier
-        const uint32_t bytes = PAIR * kABytes + static_cast<uint32_t>(tl.n_mma) * (kBK * 2);
+        const int b_land = 16 << tl.b_box;  // token rows each CTA's copy lands per k-block
+        // bytes both CTAs' copies deliver to the leader's barrier per stage
+        const uint32_t bytes =
+            static_cast<uint32_t>(PAIR * kKPS) * (kABytes + static_cast<uint32_t>(b_land) * (kBK * 2));
         const uint32_t idesc = idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma));
-        for (int kb = 0; kb < nk; ++kb) {
+        const CUtensorMap* bmap = &p.b[tl.b_src][tl.b_box];
+        for (int kb = 0; kb < nk; kb += kKPS) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
             ok = false;
@@ -495,28 +534,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           uint32_t fb = full_bar(stage);
           if (rank == 0) {
             idesc_slot[stage] = idesc;
+            boff_slot[stage] = static_cast<uint32_t>(b_land) * (kBK * 2);
             mbar_arrive_expect_tx(fb, bytes);
             armed |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           }
           if (PAIR == 2) fb = map_to_rank(fb, 0);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d<PAIR>(sa, &p.a[tl.a_sel], fb, kb * kBK, tl.a_row);
-            tma_load_2d<PAIR>(sa + kABytes / 2, &p.a3[tl.a_sel], fb, kb * kBK, tl.a_row);
-          } else {
-            tma_load_2d<PAIR>(sa, &p.a[tl.a_sel], fb, kb * kBK, tl.a_row);
-          }
-          // this CTA's token rows as boxes of 256/128/64/32/16 rows
-          int off = 0;
-#pragma unroll
-          for (int i = kNumBoxes - 1; i >= 0; --i) {
-            const int rows = 16 << i;
-            if (rows <= C::kBRows && (tl.b_rows & rows)) {
-              tma_load_2d<PAIR>(sa + kABytes + off * (kBK * 2), &p.b[tl.b_src][i], fb, kb * kBK,
-                                tl.b_row + off);
-              off += rows;
-            }
-          }
+          // weights: both k-blocks in one copy (chunk kb and kb + 1)
+          if (EPI == EPI_SWIGLU)
+            tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), kb);
+          else
+            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, kb);
+          // tokens: both k-blocks in one copy
+          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, kb);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -542,7 +572,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = 0; kb < nk; kb += kKPS) {
           if (!mbar_wait(full_bar(stage), phase)) {
             raise_device_error(DEV_ERR_TIMEOUT_MMA);
             ok = false;
@@ -550,11 +580,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           tc_fence_after();
           const uint32_t idesc = idesc_slot[stage];
+          const uint32_t boff = boff_slot[stage];
           const uint32_t sa = base + stage * C::kStageBytes;
-          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + kABytes);
+          // a chunk past the end of K was zero-filled: its MMAs add nothing
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            tc_mma<PAIR>(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          for (int c = 0; c < kKPS; ++c) {
+            const uint64_t da = sdesc_sw128(sa + c * kABytes);
+            const uint64_t db = sdesc_sw128(sa + kKPS * kABytes + c * boff);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              tc_mma<PAIR>(d_tmem, da + 2 * k, db + 2 * k, idesc, ((kb + c) | k) != 0);
+          }
           tc_commit_all<PAIR>(empty_bar(stage));  // frees the stage in both CTAs once read
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -595,14 +631,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
         const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
         if (EPI == EPI_SWIGLU) {
-          // lanes 0..63 hold the gate rows, 64..127 the matching up rows
-          if (q >= 2) {
+          // lanes 0..63 hold the gate rows and 64..127 the matching up rows
+          // (the other way round when the map lands W3 first); the warps
+          // holding up values hand them to the partner warp q ^ 2
+          const bool gate_warp = (q < 2) != (p.up_first[tl.a_sel] != 0);
+          if (!gate_warp) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]);
           }
           named_bar_sync(1, 128);
-          if (q < 2) {
-            const float* up = stage_buf + (q + 2) * 32 * 33;
+          if (gate_warp) {
+            const float* up = stage_buf + (q ^ 2) * 32 * 33;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float g = __uint_as_float(v[i]);
@@ -612,7 +651,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (row_ok) {
               __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
-                                 orow * p.out_ld + tl.out_col + q * 32;
+                                 orow * p.out_ld + tl.out_col + (q & 1) * 32;
               float r[8];
 #pragma unroll
               for (int j0 = 0; j0 < 32; j0 += 8) {
