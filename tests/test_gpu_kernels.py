@@ -175,6 +175,12 @@ FFN_SHAPES = [
     S("ffn_no_shared", T=129, H=256, n_routed=8, n_shared=0, top_k=3, inter=64),
     S("ffn_shared_only", T=77, H=256, n_routed=4, n_shared=2, top_k=0, inter=64),
     S("ffn_long_k", T=100, H=1024, n_routed=16, n_shared=1, top_k=4, inter=1408 // 4 + 32),
+    # experts with 257..511 rows (a full tile and a tail), a shared expert
+    # whose 2000 rows end in a 208-row tail, an odd number of k-blocks
+    S("ffn_wide_tiles", T=2000, H=256, n_routed=8, n_shared=1, top_k=2, inter=128),
+    S("ffn_wide_relu", T=700, H=384, n_routed=3, n_shared=1, top_k=1, inter=256,
+      act=W.ACT_RELU),
+    S("ffn_wide_odd_k", T=900, H=256, n_routed=4, n_shared=1, top_k=1, inter=192),
     dataclasses.replace(W.SHAPES["tiny_f32"], name="ffn_tiny_f32"),
     S("ffn_f32_swiglu", T=150, H=64, n_routed=5, n_shared=1, top_k=2, inter=40, dtype="f32"),
 ]
