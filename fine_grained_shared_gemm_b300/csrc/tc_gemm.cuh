@@ -209,43 +209,56 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Tiled TMA loads into this CTA's shared memory.  With PAIR == 2 the
-// completion is signalled on `bar`, a shared::cluster address that may be the
-// peer CTA's barrier.
+// Tiled TMA loads into this CTA's shared memory, with an L2 cache policy
+// (createpolicy).  With PAIR == 2 the completion is signalled on `bar`, a
+// shared::cluster address that may be the peer CTA's barrier.
 template <int PAIR>
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z) {
+                                            int x, int y, int z, uint64_t policy) {
   if (PAIR == 1)
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
   else
     asm volatile(
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 
 template <int PAIR>
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
+                                            int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t policy) {
   if (PAIR == 1)
     asm volatile(
         "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-        "r"(c4)
+        "r"(c4), "l"(policy)
         : "memory");
   else
     asm volatile(
         "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-        "r"(c4)
+        "r"(c4), "l"(policy)
         : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -409,6 +422,7 @@ struct Tile {
   int out_sel, out_row;  // output buffer and the tile's first output row
   int out_col;           // this CTA's first output column
   int n_valid;           // valid token rows of the tile
+  int nt;                // token tiles of the tile's group
 };
 
 // prefix: the tile prefix staged in shared memory (unused for a dense group).
@@ -440,6 +454,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.a_row = d.a_row0 + (w * PAIR + rank) * kCols;
   tl.n_valid = min(th, d.count - n * th);
   tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
+  tl.nt = nt;
   tl.b_rows = tl.n_mma / PAIR;
   tl.b_box = box_index(tl.b_rows);
   tl.b_src = d.b_src;
@@ -516,6 +531,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, last_parity = 0;
       bool ok = true;
+      // L2 policy: a weight tile that only one token tile reads is streamed
+      // through (evict first); one that several token tiles read, and the
+      // token rows (read by every weight tile of their group), stay (evict last)
+      const uint64_t pol_once = l2_policy_evict_first(), pol_keep = l2_policy_evict_last();
       for (int t = first; t < total && ok; t += stride) {
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
         const int b_land = 16 << tl.b_box;  // token rows each CTA's copy lands per k-block
@@ -541,12 +560,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           if (PAIR == 2) fb = map_to_rank(fb, 0);
           // weights: both k-blocks in one copy (chunk kb and kb + 1)
+          const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
           if (EPI == EPI_SWIGLU)
-            tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), kb);
+            tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), kb, pol_a);
           else
-            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, kb);
+            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, kb, pol_a);
           // tokens: both k-blocks in one copy
-          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, kb);
+          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, kb, pol_keep);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
