@@ -527,6 +527,44 @@ moe_status check_weights_ffn(const moe_shape* s, const moe_weights* w) {
   return MOE_OK;
 }
 
+// Host-buffer pipeline: how many token chunks, and the two copy streams
+// (created once per device, non-blocking, kept until the process exits).
+// A chunk keeps at least kHostChunkTokens tokens and, on average, two full
+// 256-row token tiles per routed expert: smaller chunks would add partly
+// filled tiles, each of which streams its expert's weights again.
+constexpr int kMaxHostChunks = 8;
+constexpr int kHostChunkTokens = 4096;
+constexpr int kHostChunkExpertRows = 512;
+
+int host_chunks(const moe_shape* s) {
+  int n = s->T / kHostChunkTokens;
+  if (s->top_k > 0)
+    n = std::min<long long>(n, static_cast<long long>(s->T) * s->top_k /
+                                   (static_cast<long long>(s->n_routed) * kHostChunkExpertRows));
+  return std::max(1, std::min(kMaxHostChunks, n));
+}
+
+struct CopyStreams {
+  cudaStream_t in, out;
+};
+
+moe_status copy_streams(CopyStreams* out) {
+  static std::mutex mu;
+  static CopyStreams per_dev[64];
+  static bool made[64] = {false};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!made[dev]) {
+    MOE_CUDA(cudaStreamCreateWithFlags(&per_dev[dev].in, cudaStreamNonBlocking));
+    MOE_CUDA(cudaStreamCreateWithFlags(&per_dev[dev].out, cudaStreamNonBlocking));
+    made[dev] = true;
+  }
+  *out = per_dev[dev];
+  return MOE_OK;
+}
+
 moe_status layer_forward(const moe_shape* s, const moe_weights* wt, const void* u, void* h,
                          const moe_route_outputs* ro, void* ws, size_t ws_bytes,
                          cudaStream_t st) {
@@ -674,12 +712,71 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* s, const moe_weights*
   MOE_TRY(check_shape(s));
   if (s->T > 0 && (u_host == nullptr || h_host == nullptr || !ok_ptr(u_dev) || !ok_ptr(h_dev)))
     return MOE_ERR_INVALID_ARG;
-  const size_t bytes = static_cast<size_t>(s->T) * s->H * elt_bytes(s);
+  MOE_TRY(check_weights_ffn(s, weights));
+  if (ws == nullptr || !al16(ws) || ws_bytes < carve_layer(nullptr, s).total)
+    return MOE_ERR_WORKSPACE;
   cudaStream_t st = cs(stream);
-  if (bytes) MOE_CUDA(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, st));
-  MOE_TRY(layer_forward(s, weights, u_dev, h_dev, nullptr, ws, ws_bytes, st));
-  if (bytes) MOE_CUDA(cudaMemcpyAsync(h_host, h_dev, bytes, cudaMemcpyDeviceToHost, st));
-  return MOE_OK;
+  if (s->T == 0) return MOE_OK;
+  const int n_chunks = host_chunks(s);
+  if (n_chunks == 1) {
+    const size_t bytes = static_cast<size_t>(s->T) * s->H * elt_bytes(s);
+    MOE_CUDA(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, st));
+    MOE_TRY(layer_forward(s, weights, u_dev, h_dev, nullptr, ws, ws_bytes, st));
+    MOE_CUDA(cudaMemcpyAsync(h_host, h_dev, bytes, cudaMemcpyDeviceToHost, st));
+    return MOE_OK;
+  }
+  // Token chunks in a pipeline: chunk c's host-to-device copy (stream `in`)
+  // overlaps the layer on chunk c - 1 (the caller's stream) and the copy back
+  // of chunk c - 2 (stream `out`).  Tokens are independent, so each chunk is
+  // a layer call of its own; the workspace is reused chunk after chunk on the
+  // caller's stream.
+  CopyStreams cp;
+  MOE_TRY(copy_streams(&cp));
+  cudaEvent_t ev[3 * kMaxHostChunks];
+  int n_ev = 0;
+  moe_status status = MOE_OK;
+  auto fail = [&](cudaError_t e) { status = cuda_fail(e); };
+  for (int i = 0; i < 3 * n_chunks && status == MOE_OK; ++i) {
+    const cudaError_t e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) fail(e); else n_ev = i + 1;
+  }
+  // the copy streams first wait for whatever the caller queued before this call
+  if (status == MOE_OK) {
+    cudaError_t e = cudaEventRecord(ev[0], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.in, ev[0], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.out, ev[0], 0);
+    if (e != cudaSuccess) fail(e);
+  }
+  const size_t row_bytes = static_cast<size_t>(s->H) * elt_bytes(s);
+  const int per = (s->T + n_chunks - 1) / n_chunks;
+  for (int c = 0; c < n_chunks && status == MOE_OK; ++c) {
+    const int t0 = c * per, t1 = std::min(s->T, t0 + per);
+    if (t1 <= t0) break;
+    moe_shape sc = *s;
+    sc.T = t1 - t0;
+    const size_t off = static_cast<size_t>(t0) * row_bytes, bytes = (t1 - t0) * row_bytes;
+    cudaEvent_t in_done = ev[3 * c], layer_done = ev[3 * c + 1], out_done = ev[3 * c + 2];
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(u_dev) + off,
+                                    static_cast<const char*>(u_host) + off, bytes,
+                                    cudaMemcpyHostToDevice, cp.in);
+    if (e == cudaSuccess) e = cudaEventRecord(in_done, cp.in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, in_done, 0);
+    if (e != cudaSuccess) { fail(e); break; }
+    status = layer_forward(&sc, weights, static_cast<const char*>(u_dev) + off,
+                           static_cast<char*>(h_dev) + off, nullptr, ws, ws_bytes, st);
+    if (status != MOE_OK) break;
+    e = cudaEventRecord(layer_done, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.out, layer_done, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(h_host) + off, static_cast<const char*>(h_dev) + off,
+                          bytes, cudaMemcpyDeviceToHost, cp.out);
+    if (e == cudaSuccess) e = cudaEventRecord(out_done, cp.out);
+    // the caller's stream completes only after the last copy back
+    if (e == cudaSuccess && c == n_chunks - 1) e = cudaStreamWaitEvent(st, out_done, 0);
+    if (e != cudaSuccess) fail(e);
+  }
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);  // released once they complete
+  return status;
 }
 
 // ---- moe_dispatch_static: dispatch with its scratch in a fixed array of the

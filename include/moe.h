@@ -182,9 +182,19 @@ MOE_API moe_status moe_layer_forward(const moe_shape* shape,
                                      moe_stream_t stream);
 
 /* The same layer with HOST token buffers: copies u_host [T, H] into u_dev,
- * runs moe_layer_forward, copies h_dev into h_host [T, H], all on `stream`,
- * and returns without synchronising (synchronise before reading h_host).
- * Host buffers should be pinned for the copies to be asynchronous. */
+ * runs moe_layer_forward, copies h_dev into h_host [T, H], and returns
+ * without synchronising; once `stream` has completed, h_host holds the
+ * result (synchronise `stream` before reading it).  Host buffers should be
+ * pinned for the copies to be asynchronous.
+ * Large batches are pipelined: the tokens are cut into up to 8 chunks (each
+ * at least 4096 tokens and, on average, at least 512 rows per routed expert)
+ * and the copy of one chunk to the device, the layer on the previous chunk
+ * and the copy back of the one before run at the same time.  The copies run
+ * on two non-blocking streams that the library creates on the first such
+ * call on a device and keeps; they wait for the work queued on `stream`
+ * before the call, and `stream` waits for the last copy back.  The result is
+ * bitwise the same as one moe_layer_forward over all tokens (tokens are
+ * independent).  ws: moe_layer_workspace_size(shape) bytes. */
 MOE_API moe_status moe_layer_forward_host(const moe_shape* shape,
                                           const moe_weights* weights,
                                           const void* u_host, void* h_host,

@@ -115,6 +115,23 @@ def test_layer_host_buffers_match_device_path():
     assert torch.equal(h_host, h_dev_path.cpu())
 
 
+def test_layer_host_buffers_pipelined_chunks_match_device_path():
+    # enough tokens for the host-buffer entry point to pipeline three chunks
+    # (copies on their own streams overlapping the layer on earlier chunks)
+    shape = W.MoEShape("host_chunks", T=3 * 4096 + 100, H=256, n_routed=16, n_shared=1,
+                       top_k=4, inter=128, gate=W.GATE_SIGMOID_BIAS, bias_range=0.1)
+    inp = W.make_inputs(shape, DEV, seed=6)
+    h_dev_path, _ = run_layer(shape, inp)
+    ws, h = layer_buffers(shape, DEV)
+    u_host = inp.u.cpu().pin_memory()
+    h_host = torch.zeros_like(u_host).pin_memory()
+    u_dev = torch.empty_like(inp.u)
+    M.moe_layer_forward_host(shape, M.weights_struct(inp), u_host, h_host, u_dev, h, ws)
+    torch.cuda.synchronize()
+    assert M.moe_device_status()[0] == M.MOE_OK
+    assert torch.equal(h_host, h_dev_path.cpu())
+
+
 # full-size page-shaped layers: (shape name, sampled tokens)
 FULL = [("dsmoe16b_bf16", 48), ("v3_prefill_bf16", 12), ("decode_bf16", 8),
         ("v3_prefill_e32_bf16", 16), ("sweep_m16_e32_bf16", 24)] + \
