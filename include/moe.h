@@ -37,8 +37,10 @@
  *
  * Limits: 1 ≤ n_routed + n_shared ≤ 1024; 0 ≤ top_k ≤ min(32, n_routed);
  * H % 8 == 0 and inter % 8 == 0.  bf16 additionally needs H % 128 == 0 and
- * inter % 64 (SwiGLU) or inter % 128 (ReLU) == 0; otherwise
- * MOE_ERR_UNSUPPORTED.
+ * inter % 64 (SwiGLU) or inter % 128 (ReLU) == 0, and for SwiGLU the gate
+ * and up stacks (w1 and w3, sw1 and sw3) must start at different addresses
+ * less than 2^40 bytes apart (the kernel reads them through one tensor map
+ * that steps from one to the other); otherwise MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
