@@ -102,12 +102,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 moe_status encode(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
-                  const cuuint64_t* strides, const cuuint32_t* box) {
+                  const cuuint64_t* strides, const cuuint32_t* box,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cuda_fail(cudaErrorNotSupported);
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
 }
@@ -141,6 +142,15 @@ moe_status make_map5_gate_up(CUtensorMap* m, const void* w1, const void* w3, uin
                                  tc::kBK * 2};
   const cuuint32_t box[5] = {static_cast<cuuint32_t>(tc::kBK), 64, 2, 1, tc::kKPS};
   return encode(m, 5, b < a ? w3 : w1, dims, strides, box);
+}
+
+// bf16 output [rows, cols] row-major for the epilogue's bulk stores: box of
+// 32 columns x 32 rows, plain row-major tile in shared memory.
+moe_status make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, 32};
+  return encode(m, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Token-source maps for every box height.
@@ -469,6 +479,8 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   p.n_wtiles = cdiv(I, static_cast<int>(a1_box) * pair);
   p.num_k_blocks = cdiv(H, tc::kBK);
   p.out[0] = p.out[1] = f.act;
+  MOE_TRY(make_out_map(&p.omap[0], f.act, rows_act, I));
+  p.omap[1] = p.omap[0];
   p.out_ld = I;
   p.out_cols = I;
   if (swiglu) MOE_TRY(launch_ffn<tc::EPI_SWIGLU>(p, bn, st));
@@ -489,6 +501,8 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   q.num_k_blocks = cdiv(I, tc::kBK);
   q.out[0] = Tk ? y_perm : y_shared;
   q.out[1] = Ks ? y_shared : y_perm;
+  MOE_TRY(make_out_map(&q.omap[0], q.out[0], Tk ? Tk : static_cast<uint64_t>(Ks) * T, H));
+  MOE_TRY(make_out_map(&q.omap[1], q.out[1], Ks ? static_cast<uint64_t>(Ks) * T : Tk, H));
   q.out_ld = H;
   q.out_cols = H;
   return launch_ffn<tc::EPI_BF16>(q, bn, st);

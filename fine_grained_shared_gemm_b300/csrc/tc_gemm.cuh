@@ -28,8 +28,8 @@
 // Roles (192 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocation and (leader only) MMA issue (one thread)
-//   warps 2..5  epilogue: TMEM -> registers -> shared-memory transpose ->
-//               global, with the FFN activation fused in
+//   warps 2..5  epilogue: TMEM -> registers (activation fused in) -> bf16
+//               tile in shared memory -> TMA bulk store
 //
 // The producer hands the MMA thread each stage's instruction descriptor
 // through shared memory, so the MMA thread never decodes tiles; the per-group
@@ -89,6 +89,7 @@ struct Params {
   int out_cols;                  // valid output columns
   const float* col_offset;       // EPI_F32: per-column addend, may be null
   int up_first[2];               // SwiGLU, per stack: the 5-D map lands the up rows first
+  CUtensorMap omap[2];           // bf16 outputs out[0], out[1]: 2-D, box 32 columns x 32 rows
 };
 
 constexpr int kMaxGroups = 1024;
@@ -100,7 +101,7 @@ struct Config {
   static constexpr int kBBytes = kBRows * kBK * 2;      // one k-block of tokens
   static constexpr int kStageBytes = kKPS * (kABytes + kBBytes);
   static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
-  static constexpr int kPrefixBytes = (kMaxGroups + 4) * 4;
+  static constexpr int kPrefixBytes = ((kMaxGroups + 4) * 4 + 127) / 128 * 128;
   static constexpr int kEpiBytes = kStageBufFloats * 4;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
@@ -247,6 +248,29 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
         "r"(c4), "l"(policy)
         : "memory");
+}
+
+// Bulk tensor store of a 32 x 32 bf16 box from this CTA's shared memory.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until at most N committed groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -633,6 +657,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tempty_leader1 = PAIR == 2 ? map_to_rank(tempty_bar(1), 0) : tempty_bar(1);
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t n_stores = 0;  // bulk stores this warp has issued (selects the staging buffer)
     for (int t = first; t < total; t += stride) {
       const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
       const bool ready = mbar_wait(tfull_bar(acc), acc_phase);
@@ -648,12 +673,41 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tacc + c0, v);
-        const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
-        const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
+        const int nrow = min(32, tl.n_valid - c0);  // token rows of this chunk
+        // A full chunk of 32 tokens goes out as one bulk store from a bf16
+        // tile in this warp's shared memory (two buffers, alternating; the
+        // store issued two chunks ago must have read the buffer); a partial
+        // chunk is stored from registers, so no box writes past the group.
+        auto emit = [&](auto value_of, int col_base) {
+          if (!cols_ok) return;
+          if (nrow == 32) {
+            uint16_t* stg = reinterpret_cast<uint16_t*>(buf) + (n_stores & 1) * 1024;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(value_of(j)));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.omap[tl.out_sel], smem_u32(stg), tl.out_col + col_base,
+                           tl.out_row + c0);
+              bulk_commit();
+            }
+            ++n_stores;
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
+                               static_cast<size_t>(tl.out_row + c0) * p.out_ld + tl.out_col +
+                               col_base + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nrow) o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(value_of(j));
+          }
+        };
         if (EPI == EPI_SWIGLU) {
           // lanes 0..63 hold the gate rows and 64..127 the matching up rows
           // (the other way round when the map lands W3 first); the warps
-          // holding up values hand them to the partner warp q ^ 2
+          // holding up values hand them (fp32) to the partner warp q ^ 2
           const bool gate_warp = (q < 2) != (p.up_first[tl.a_sel] != 0);
           if (!gate_warp) {
 #pragma unroll
@@ -662,27 +716,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           named_bar_sync(1, 128);
           if (gate_warp) {
             const float* up = stage_buf + (q ^ 2) * 32 * 33;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float g = __uint_as_float(v[i]);
-              const float silu = __fdividef(g, 1.0f + __expf(-g));
-              buf[i * 33 + lane] = silu * up[i * 33 + lane];
-            }
-            __syncwarp();
-            if (row_ok) {
-              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
-                                 orow * p.out_ld + tl.out_col + (q & 1) * 32;
-              float r[8];
-#pragma unroll
-              for (int j0 = 0; j0 < 32; j0 += 8) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = buf[lane * 33 + j0 + j];
-                Vec16<__nv_bfloat16>::store(o + j0, r);
-              }
-            }
+            emit([&](int j) {
+              const float g = __uint_as_float(v[j]);
+              return __fdividef(g, 1.0f + __expf(-g)) * up[j * 33 + lane];
+            }, (q & 1) * 32);
           }
           named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
+          const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
+          const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
           const int col = tl.out_col + q * 32 + lane;
           const float add =
               (p.col_offset != nullptr && col < p.out_cols) ? __ldg(p.col_offset + col) : 0.0f;
@@ -698,25 +740,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           __syncwarp();
         } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x = __uint_as_float(v[i]);
-            if (EPI == EPI_RELU) x = fmaxf(x, 0.0f);
-            buf[i * 33 + lane] = x;
-          }
-          __syncwarp();
-          if (row_ok) {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
-                               orow * p.out_ld + tl.out_col + q * 32;
-            float r[8];
-#pragma unroll
-            for (int j0 = 0; j0 < 32; j0 += 8) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) r[j] = buf[lane * 33 + j0 + j];
-              Vec16<__nv_bfloat16>::store(o + j0, r);
-            }
-          }
-          __syncwarp();
+          emit([&](int j) {
+            const float x = __uint_as_float(v[j]);
+            return EPI == EPI_RELU ? fmaxf(x, 0.0f) : x;
+          }, q * 32);
         }
       }
       // this warp has read the accumulator: tell the leader's MMA issuer
@@ -729,6 +756,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // every bulk store has completed before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
