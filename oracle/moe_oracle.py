@@ -200,6 +200,36 @@ def dispatch(idx: np.ndarray, n_routed: int):
 
 
 # --------------------------------------------------------------------------
+# Load balancing without an auxiliary loss ([CH7] §7.4)
+# --------------------------------------------------------------------------
+
+def expert_loads(idx: np.ndarray, n_routed: int) -> np.ndarray:
+    """Tokens routed to each expert in one step (every (token, slot) counts once)."""
+    return np.bincount(np.asarray(idx, np.int64).reshape(-1), minlength=n_routed)
+
+
+def update_select_bias(loads: np.ndarray, select_bias: np.ndarray, gamma: float,
+                       routed_rows: int) -> np.ndarray:
+    """One step of the per-expert bias controller of [CH7] §7.4.
+
+    After a step each expert's load is compared with the mean load
+    routed_rows / E (routed_rows = T·k): an overloaded expert's bias is lowered
+    by the step gamma, an underloaded expert's bias is raised by gamma, an
+    expert exactly at the mean keeps its bias.  The pages give no value for
+    gamma (FG §5 calls it a step coupled to the score scale): it is a
+    parameter.  Returned in float32, the type the router adds it in.
+    """
+    loads = np.asarray(loads, np.int64)
+    E = loads.shape[0]
+    over = loads * E > routed_rows           # load_i > mean, compared exactly
+    under = loads * E < routed_rows
+    b = np.asarray(select_bias, np.float64).copy()
+    b[over] -= float(np.float32(gamma))
+    b[under] += float(np.float32(gamma))
+    return b.astype(np.float32)
+
+
+# --------------------------------------------------------------------------
 # Expert FFN and combine ([PS]; [FG] Eq. 9–11)
 # --------------------------------------------------------------------------
 

@@ -282,12 +282,44 @@ def check_dispatch(o):
         assert d["counts"][e] == sum(1 for t in range(T) if e in idx[t])
 
 
-CHECKS = [check_routing_handworked, check_ffn_handworked, check_combinations]
+def check_bias_update_handworked(o, golden_dir):
+    for c in _load(golden_dir, "bias_update_handworked.json")["cases"]:
+        got = o.update_select_bias(np.array(c["loads"]), _f32(c["bias"]), c["gamma"],
+                                   c["routed_rows"])
+        assert got.dtype == np.float32
+        assert np.array_equal(got, _f32(c["expected"])), (c, got)
+
+
+def check_bias_controller_balances(o):
+    """[CH7] §7.4: the bias controller exists to even out expert loads.  A
+    router whose centroids have very different norms sends most tokens to a
+    few experts; repeated steps of route -> loads -> bias update must bring
+    the most loaded expert close to the mean and keep the loads summing to
+    T·k (the bias never changes how many experts a token gets)."""
+    rng = np.random.default_rng(3)
+    T, H, E, k = 2048, 32, 16, 2
+    u = rng.standard_normal((T, H))
+    cents = rng.standard_normal((E, H)) * np.linspace(0.02, 0.4, E)[:, None]
+    z = o.router_logits(u, cents)
+    bias = np.zeros(E, np.float32)
+    imbalance = []
+    for _ in range(300):
+        r = o.route(z, o.SIGMOID_BIAS, k, bias)
+        loads = o.expert_loads(r["idx"], E)
+        assert loads.sum() == T * k
+        imbalance.append(loads.max() * E / (T * k))
+        bias = o.update_select_bias(loads, bias, 0.002, T * k)
+    assert imbalance[0] > 1.6, imbalance[0]          # the router starts skewed
+    assert max(imbalance[-20:]) < 1.1, imbalance[-20:]
+
+
+CHECKS = [check_routing_handworked, check_ffn_handworked, check_combinations,
+          check_bias_update_handworked]
 PLAIN_CHECKS = [check_topk_bruteforce, check_softmax_properties,
                 check_softmax_choice_is_score_order, check_sigmoid_properties,
                 check_segmentation_identity, check_ffn_bruteforce,
                 check_classic_moe, check_shared_equals_forced_routed,
-                check_combine_zero_gates, check_dispatch]
+                check_combine_zero_gates, check_dispatch, check_bias_controller_balances]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -375,7 +407,17 @@ def test_planted_mistakes(golden_dir):
     def sigmoid_sign(z):
         return 1.0 / (1.0 + np.exp(np.asarray(z, np.float64)))
 
+    def bias_sign_flipped(loads, select_bias, gamma, routed_rows):
+        return O.update_select_bias(loads, select_bias, -gamma, routed_rows)
+
+    def bias_mean_over_tokens(loads, select_bias, gamma, routed_rows):
+        # mean taken as T instead of T·k (k = 2 in the controller check)
+        return O.update_select_bias(loads, select_bias, gamma, routed_rows // 2)
+
     cases = [
+        (dict(update_select_bias=bias_sign_flipped), check_bias_update_handworked, (golden_dir,)),
+        (dict(update_select_bias=bias_sign_flipped), check_bias_controller_balances, ()),
+        (dict(update_select_bias=bias_mean_over_tokens), check_bias_controller_balances, ()),
         (dict(route=renormalised_softmax), check_routing_handworked, (golden_dir,)),
         (dict(topk_by_rank=ties_to_higher), check_topk_bruteforce, ()),
         (dict(combine=no_residual), check_ffn_handworked, (golden_dir,)),
