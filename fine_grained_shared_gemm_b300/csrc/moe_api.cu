@@ -14,6 +14,7 @@
 
 #include "moe.h"
 
+#include "balance.cuh"
 #include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
@@ -711,6 +712,20 @@ MOE_API moe_status moe_combine(const moe_shape* s, const void* u, const void* y_
     return MOE_ERR_INVALID_ARG;
   if (s->n_shared > 0 && s->T > 0 && !ok_ptr(y_shared)) return MOE_ERR_INVALID_ARG;
   return do_combine(s, u, y_perm, y_shared, topk_w, slot_row, h, cs(stream));
+}
+
+MOE_API moe_status moe_update_select_bias(const moe_shape* s, const int32_t* expert_offsets,
+                                          float* select_bias, float gamma, int32_t* loads,
+                                          moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_ptr(expert_offsets) || !ok_ptr(select_bias) || !ok_opt(loads))
+    return MOE_ERR_INVALID_ARG;
+  if (!(gamma >= 0.0f) || gamma == INFINITY) return MOE_ERR_INVALID_ARG;  // also rejects NaN
+  const int E = s->n_routed;
+  bias_update_kernel<<<cdiv(E, 256), 256, 0, cs(stream)>>>(
+      expert_offsets, E, static_cast<long long>(s->T) * s->top_k, gamma, select_bias, loads);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
 }
 
 MOE_API moe_status moe_layer_forward(const moe_shape* s, const moe_weights* weights,

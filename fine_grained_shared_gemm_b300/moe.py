@@ -72,6 +72,7 @@ _SIGNATURES = {
                                          _P, ctypes.c_size_t, _P]),
     "moe_layer_forward_host": (ctypes.c_int, [_S, _W, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch_static": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_update_select_bias": (ctypes.c_int, [_S, _P, _P, ctypes.c_float, _P, _P]),
 }
 
 _lib = None
@@ -179,6 +180,14 @@ def moe_dispatch_static(shape, topk_idx, u, expert_offsets, row_token, slot_row,
     _check("moe_dispatch_static", lib().moe_dispatch_static(
         ctypes.byref(shape_struct(shape)), _ptr(topk_idx), _ptr(u), _ptr(expert_offsets),
         _ptr(row_token), _ptr(slot_row), _ptr(u_perm), _stream(stream)))
+
+
+def moe_update_select_bias(shape, expert_offsets, select_bias, gamma: float, loads=None,
+                           stream=None):
+    """One step of the aux-loss-free bias controller, in place on select_bias."""
+    _check("moe_update_select_bias", lib().moe_update_select_bias(
+        ctypes.byref(shape_struct(shape)), _ptr(expert_offsets), _ptr(select_bias),
+        ctypes.c_float(gamma), _ptr(loads), _stream(stream)))
 
 
 def moe_expert_ffn(shape, weights: moe_weights, u, u_perm, expert_offsets, y_perm, y_shared,

@@ -174,6 +174,20 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const void* u,
                                const float* topk_w, const int32_t* slot_row,
                                void* h, moe_stream_t stream);
 
+/* Selection-bias controller of the aux-loss-free load balancing (page "MoE
+ * 的分水岭", ibossgateway ch. 7 §7.4): for every routed expert e, its load
+ * L_e = expert_offsets[e+1] - expert_offsets[e] (the rows moe_dispatch gave
+ * it) is compared with the mean load T·k / E (exactly, in integers);
+ * select_bias[e] -= gamma if L_e is above the mean, += gamma if below, and
+ * stays if equal (one fp32 rounding).  select_bias [E] fp32 is updated in
+ * place; loads [E] int32 (may be NULL) receives L_e.  gamma >= 0 and finite
+ * (the pages give no value; it is the caller's step).  The bias is the one
+ * MOE_GATE_SIGMOID_BIAS adds for the choice only. */
+MOE_API moe_status moe_update_select_bias(const moe_shape* shape,
+                                          const int32_t* expert_offsets,
+                                          float* select_bias, float gamma,
+                                          int32_t* loads, moe_stream_t stream);
+
 /* Whole layer: router logits, route, dispatch, expert FFNs, combine, all on
  * `stream`.  route_out (may be NULL) receives copies of the routing
  * intermediates.  ws: moe_layer_workspace_size bytes. */

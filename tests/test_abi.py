@@ -109,3 +109,16 @@ def test_workspace_too_small_rejected():
     need_d = L.moe_dispatch_workspace_size(ctypes.byref(s))
     assert L.moe_dispatch(ctypes.byref(s), 256, 256, 256, 256, 256, 256, 256, need_d - 1,
                           None) == M.MOE_ERR_WORKSPACE
+
+
+def test_bias_update_rejects_bad_gamma_and_pointers():
+    s = _shape()
+    L = M.lib()
+    f = ctypes.c_float
+    for g in (-0.1, float("nan"), float("inf")):
+        assert L.moe_update_select_bias(ctypes.byref(s), 256, 256, f(g), None, None) == \
+            M.MOE_ERR_INVALID_ARG, g
+    assert L.moe_update_select_bias(ctypes.byref(s), None, 256, f(0.1), None, None) == \
+        M.MOE_ERR_INVALID_ARG
+    assert L.moe_update_select_bias(ctypes.byref(s), 256, 258, f(0.1), None, None) == \
+        M.MOE_ERR_INVALID_ARG
