@@ -150,29 +150,64 @@ def selection_key(z: np.ndarray, gate: str,
     raise ValueError(gate)
 
 
+def group_choice(group_key: np.ndarray, n_groups: int, topk_groups: int):
+    """Node/group-limited routing, first stage ([FG] §4): the E routed experts
+    form n_groups groups of E / n_groups consecutive experts; a group's score
+    is the sum of its experts' scores (float64); the topk_groups best groups
+    are kept, ties to the lower group index.  Returns (allowed [T,E] bool,
+    gap [T]: the topk_groups-th minus the next group score, +inf if all kept).
+    """
+    group_key = np.asarray(group_key, np.float64)
+    T, E = group_key.shape
+    gs = E // n_groups
+    gsum = group_key.reshape(T, n_groups, gs).sum(axis=2)
+    gidx = topk_by_rank(gsum, min(topk_groups + 1, n_groups))
+    allowed = np.zeros((T, n_groups), dtype=bool)
+    np.put_along_axis(allowed, gidx[:, :topk_groups], True, axis=1)
+    gap = np.full(T, np.inf)
+    if topk_groups < n_groups:
+        rows = np.arange(T)
+        gap = gsum[rows, gidx[:, topk_groups - 1]] - gsum[rows, gidx[:, topk_groups]]
+    return np.repeat(allowed, gs, axis=1), gap
+
+
 def route(z: np.ndarray, gate: str, top_k: int,
-          select_bias: Optional[np.ndarray] = None):
+          select_bias: Optional[np.ndarray] = None, n_groups: int = 0,
+          topk_groups: int = 0):
     """Scores, choice and gate weights for every token.
 
     Returns dict(idx [T,k] int64, weights [T,k] float64, scores [T,E] float64,
-    key [T,E], gap [T] float64).  gap is the k-th minus the (k+1)-th largest
-    score (softmax) or key (sigmoid + bias); +inf when k equals E.
+    key [T,E], gap [T] float64, group_gap [T]).  gap is the k-th minus the
+    (k+1)-th largest score (softmax) or key (sigmoid + bias) among the experts
+    the token may choose; +inf when there is no (k+1)-th.  With n_groups > 0
+    the choice is group-limited ([FG] §4): groups are scored by the sum of the
+    scores the choice is made on — the softmax scores, or the keys s + b —
+    and only experts of the topk_groups best groups may be chosen; group_gap
+    is the margin of the last kept group (+inf without groups).
     """
     z = np.asarray(z, np.float32)
     T, E = z.shape
     scores = softmax_scores(z) if gate == SOFTMAX else sigmoid_scores(z)
     key = selection_key(z, gate, select_bias)
-    idx = topk_by_rank(key, min(top_k + 1, E))
+    group_gap = np.full(T, np.inf)
+    choice_key = key
+    if n_groups > 0:
+        allowed, group_gap = group_choice(scores if gate == SOFTMAX else key,
+                                          n_groups, topk_groups)
+        choice_key = np.where(allowed, key, np.float32(-np.inf))
+    idx = topk_by_rank(choice_key, min(top_k + 1, E))
     gap = np.full(T, np.inf)
     if 0 < top_k < E:
         rows = np.arange(T)
         gap_src = scores if gate == SOFTMAX else key.astype(np.float64)
-        gap = gap_src[rows, idx[:, top_k - 1]] - gap_src[rows, idx[:, top_k]]
+        nxt = idx[:, top_k]
+        has_next = np.isfinite(choice_key[rows, nxt])
+        gap = np.where(has_next, gap_src[rows, idx[:, top_k - 1]] - gap_src[rows, nxt], np.inf)
     idx = idx[:, :top_k]
     g = np.take_along_axis(scores, idx, axis=1)
     if gate == SIGMOID_BIAS and top_k > 0:
         g = g / g.sum(axis=1, keepdims=True)     # [FG] Eq. 15, raw scores only
-    return dict(idx=idx, weights=g, scores=scores, key=key, gap=gap)
+    return dict(idx=idx, weights=g, scores=scores, key=key, gap=gap, group_gap=group_gap)
 
 
 # --------------------------------------------------------------------------

@@ -313,13 +313,53 @@ def check_bias_controller_balances(o):
     assert max(imbalance[-20:]) < 1.1, imbalance[-20:]
 
 
+def check_group_routing_handworked(o, golden_dir):
+    g = _load(golden_dir, "group_routing_handworked.json")
+    keys = _f32(g["keys"])
+    bias = (keys - np.float32(0.5)).astype(np.float32)   # sigmoid(0) = 0.5 exactly
+    z = np.zeros((1, keys.shape[0]), np.float32)
+    for c in g["cases"]:
+        r = o.route(z, o.SIGMOID_BIAS, c["top_k"], bias, g["n_groups"], c["topk_groups"])
+        assert r["idx"][0].tolist() == c["idx"], (c, r["idx"])
+        assert np.allclose(r["weights"], 1.0 / c["top_k"])
+
+
+def check_group_routing_bruteforce(o):
+    """Chosen groups maximise the summed group score over all group subsets,
+    chosen experts maximise the summed key over all subsets of their experts
+    (random keys, no ties); keeping every group is plain top-k; one expert
+    per group with as many groups as k chooses the plain top-k set."""
+    rng = np.random.default_rng(7)
+    E, G, M, k = 12, 4, 2, 3
+    gs = E // G
+    for gate in (o.SOFTMAX, o.SIGMOID_BIAS):
+        z = rng.standard_normal((40, E)).astype(np.float32)
+        bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+        r = o.route(z, gate, k, bias, G, M)
+        gkey = r["scores"] if gate == o.SOFTMAX else r["key"].astype(np.float64)
+        for t in range(z.shape[0]):
+            gsum = gkey[t].reshape(G, gs).sum(axis=1)
+            best_groups = max(itertools.combinations(range(G), M),
+                              key=lambda c: sum(gsum[list(c)]))
+            pool = [e for gg in best_groups for e in range(gg * gs, gg * gs + gs)]
+            best = max(itertools.combinations(pool, k),
+                       key=lambda c: sum(float(r["key"][t, e]) for e in c))
+            assert sorted(r["idx"][t].tolist()) == sorted(best), (gate, t)
+        plain = o.route(z, gate, k, bias)
+        assert np.array_equal(o.route(z, gate, k, bias, G, G)["idx"], plain["idx"])
+        if gate == o.SIGMOID_BIAS:
+            one = o.route(z, gate, k, bias, E, k)
+            assert np.array_equal(np.sort(one["idx"], 1), np.sort(plain["idx"], 1))
+
+
 CHECKS = [check_routing_handworked, check_ffn_handworked, check_combinations,
-          check_bias_update_handworked]
+          check_bias_update_handworked, check_group_routing_handworked]
 PLAIN_CHECKS = [check_topk_bruteforce, check_softmax_properties,
                 check_softmax_choice_is_score_order, check_sigmoid_properties,
                 check_segmentation_identity, check_ffn_bruteforce,
                 check_classic_moe, check_shared_equals_forced_routed,
-                check_combine_zero_gates, check_dispatch, check_bias_controller_balances]
+                check_combine_zero_gates, check_dispatch, check_bias_controller_balances,
+                check_group_routing_bruteforce]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -414,7 +454,18 @@ def test_planted_mistakes(golden_dir):
         # mean taken as T instead of T·k (k = 2 in the controller check)
         return O.update_select_bias(loads, select_bias, gamma, routed_rows // 2)
 
+    def group_by_max(group_key, n_groups, topk_groups):
+        gk = np.asarray(group_key, np.float64)
+        T, E = gk.shape
+        gmax = gk.reshape(T, n_groups, E // n_groups).max(axis=2)
+        gidx = O.topk_by_rank(gmax, topk_groups)
+        allowed = np.zeros((T, n_groups), dtype=bool)
+        np.put_along_axis(allowed, gidx, True, axis=1)
+        return np.repeat(allowed, E // n_groups, axis=1), np.full(T, np.inf)
+
     cases = [
+        (dict(group_choice=group_by_max), check_group_routing_handworked, (golden_dir,)),
+        (dict(group_choice=group_by_max), check_group_routing_bruteforce, ()),
         (dict(update_select_bias=bias_sign_flipped), check_bias_update_handworked, (golden_dir,)),
         (dict(update_select_bias=bias_sign_flipped), check_bias_controller_balances, ()),
         (dict(update_select_bias=bias_mean_over_tokens), check_bias_controller_balances, ()),
