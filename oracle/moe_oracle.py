@@ -181,7 +181,8 @@ def route(z: np.ndarray, gate: str, top_k: int,
     (k+1)-th largest score (softmax) or key (sigmoid + bias) among the experts
     the token may choose; +inf when there is no (k+1)-th.  With n_groups > 0
     the choice is group-limited ([FG] §4): groups are scored by the sum of the
-    scores the choice is made on — the softmax scores, or the keys s + b —
+    scores the choice is made on — the softmax scores rounded to fp32, or the
+    fp32 keys s + b —
     and only experts of the topk_groups best groups may be chosen; group_gap
     is the margin of the last kept group (+inf without groups).
     """
@@ -192,8 +193,10 @@ def route(z: np.ndarray, gate: str, top_k: int,
     group_gap = np.full(T, np.inf)
     choice_key = key
     if n_groups > 0:
-        allowed, group_gap = group_choice(scores if gate == SOFTMAX else key,
-                                          n_groups, topk_groups)
+        # the group decision is taken in the kernel's precision: fp32 scores
+        # (softmax) or the fp32 keys, summed in float64
+        gkey = scores.astype(np.float32) if gate == SOFTMAX else key
+        allowed, group_gap = group_choice(gkey, n_groups, topk_groups)
         choice_key = np.where(allowed, key, np.float32(-np.inf))
     idx = topk_by_rank(choice_key, min(top_k + 1, E))
     gap = np.full(T, np.inf)

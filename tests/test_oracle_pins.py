@@ -336,7 +336,7 @@ def check_group_routing_bruteforce(o):
         z = rng.standard_normal((40, E)).astype(np.float32)
         bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
         r = o.route(z, gate, k, bias, G, M)
-        gkey = r["scores"] if gate == o.SOFTMAX else r["key"].astype(np.float64)
+        gkey = (r["scores"].astype(np.float32) if gate == o.SOFTMAX else r["key"]).astype(np.float64)
         for t in range(z.shape[0]):
             gsum = gkey[t].reshape(G, gs).sum(axis=1)
             best_groups = max(itertools.combinations(range(G), M),
