@@ -60,6 +60,15 @@ moe_status check_shape(const moe_shape* s) {
   if (s->act != MOE_ACT_RELU && s->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (s->dtype != MOE_DTYPE_F32 && s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (s->n_routed + s->n_shared > 1024 || s->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (s->n_groups < 0 || s->topk_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (s->n_groups > 0) {
+    if (s->n_groups > 32) return MOE_ERR_UNSUPPORTED;
+    if (s->n_routed % s->n_groups != 0 || s->topk_groups < 1 || s->topk_groups > s->n_groups ||
+        s->topk_groups * (s->n_routed / s->n_groups) < s->top_k)
+      return MOE_ERR_INVALID_ARG;
+  } else if (s->topk_groups != 0) {
+    return MOE_ERR_INVALID_ARG;
+  }
   if (s->H % 8 != 0 || s->inter % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (s->dtype == MOE_DTYPE_BF16) {
     if (s->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -352,7 +361,9 @@ moe_status do_route(const moe_shape* s, const float* logits, const float* bias, 
   const int blocks = route_blocks(T);
   const int npl = cdiv(E, 32);
   const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
-#define MOE_ROUTE(N) route_kernel<N><<<blocks, 256, 0, st>>>(logits, bias, T, E, s->top_k, gate, idx, w, gap)
+#define MOE_ROUTE(N)                                                                     \
+  route_kernel<N><<<blocks, 256, 0, st>>>(logits, bias, T, E, s->top_k, gate, s->n_groups, \
+                                          s->topk_groups, idx, w, gap)
   if (npl <= 1) MOE_ROUTE(1);
   else if (npl <= 2) MOE_ROUTE(2);
   else if (npl <= 4) MOE_ROUTE(4);

@@ -9,6 +9,11 @@
 // the raw s_i of the chosen divided by their sum.
 // Ties go to the lower expert index.  The sum reductions use a fixed
 // butterfly order, so the result does not depend on scheduling.
+// Group-limited routing (§4, node-limited routing): with n_groups > 0 the
+// experts form groups of E / n_groups consecutive indices; a group's score is
+// the sum (float64) of its experts' softmax scores, or keys s + b; the
+// topk_groups best groups are kept (ties to the lower group index) and the
+// top-k is taken among their experts only.
 #pragma once
 
 #include <math_constants.h>
@@ -45,6 +50,12 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
@@ -56,7 +67,8 @@ __device__ __forceinline__ float warp_max(float x) {
 template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
                                                     const float* __restrict__ bias, int T,
-                                                    int E, int k, int gate,
+                                                    int E, int k, int gate, int n_groups,
+                                                    int topk_groups,
                                                     int32_t* __restrict__ topk_idx,
                                                     float* __restrict__ topk_w,
                                                     float* __restrict__ kth_gap) {
@@ -97,6 +109,40 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
       }
     }
 
+    if (n_groups > 0) {
+      // lane g ends up holding group g's score
+      const int gs = E / n_groups;
+      double my_group = -CUDART_INF;
+      for (int g = 0; g < n_groups; ++g) {
+        double part = 0.0;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && e / gs == g) part += static_cast<double>(gate == 0 ? score[i] : key[i]);
+        }
+        const double sum = warp_sum_f64(part);
+        if (lane == g) my_group = sum;
+      }
+      uint32_t keep = 0;  // bit g: group g kept
+      for (int r = 0; r < topk_groups; ++r) {
+        double best = my_group;
+        int best_g = lane < n_groups && !((keep >> lane) & 1u) ? lane : 0x7fffffff;
+        if (best_g == 0x7fffffff) best = -CUDART_INF;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const double ob = __shfl_xor_sync(0xffffffffu, best, off);
+          const int og = __shfl_xor_sync(0xffffffffu, best_g, off);
+          if (ob > best || (ob == best && og < best_g)) { best = ob; best_g = og; }
+        }
+        keep |= 1u << best_g;
+      }
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((keep >> (e / gs)) & 1u)) key[i] = -CUDART_INF_F;
+      }
+    }
+
     uint32_t taken = 0;
     float my_score = 0.0f;
     int my_idx = 0;
@@ -125,7 +171,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
             b = Best{key[i], score[i], e};
         }
         b = warp_best(b);
-        gap = (gate == 0) ? last.score - b.score : last.key - b.key;
+        // no (k+1)-th expert among the kept groups: no competitor
+        gap = b.key == -CUDART_INF_F ? CUDART_INF_F
+                                      : (gate == 0) ? last.score - b.score : last.key - b.key;
       }
       if (lane == 0) kth_gap[t] = gap;
     }

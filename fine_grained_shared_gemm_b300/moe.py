@@ -39,7 +39,8 @@ class MoEError(RuntimeError):
 
 class moe_shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("T", "H", "n_routed", "n_shared", "top_k", "inter", "gate", "act", "dtype")]
+                ("T", "H", "n_routed", "n_shared", "top_k", "inter", "gate", "act", "dtype",
+                 "n_groups", "topk_groups")]
 
 
 class moe_weights(ctypes.Structure):
@@ -102,7 +103,8 @@ def shape_struct(s) -> moe_shape:
     if isinstance(s, moe_shape):
         return s
     return moe_shape(s.T, s.H, s.n_routed, s.n_shared, s.top_k, s.inter,
-                     GATE_CODES[s.gate], ACT_CODES[s.act], DTYPE_CODES[s.dtype])
+                     GATE_CODES[s.gate], ACT_CODES[s.act], DTYPE_CODES[s.dtype],
+                     s.n_groups, s.topk_groups)
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -64,6 +64,10 @@ class MoEShape:
     dtype: str = "bf16"
     bias_range: float = 0.0          # b_i ~ U(-bias_range, bias_range); 0 = no bias
     logit_offset_std: float = 0.0    # o_i ~ N(0, std^2); 0 = no offset
+    # group-limited routing: n_groups groups of n_routed / n_groups experts,
+    # topk_groups of them kept per token; 0 = no limit
+    n_groups: int = 0
+    topk_groups: int = 0
     # Segmentation provenance (None where the shape is quoted directly):
     # N base FFNs of width M, granularity m, K active base FFNs.
     seg: Optional[tuple] = field(default=None)

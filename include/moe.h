@@ -41,6 +41,9 @@
  * and up stacks (w1 and w3, sw1 and sw3) must start at different addresses
  * less than 2^40 bytes apart (the kernel reads them through one tensor map
  * that steps from one to the other); otherwise MOE_ERR_UNSUPPORTED.
+ * Group-limited routing needs 1 <= n_groups <= 32, n_routed % n_groups == 0,
+ * 1 <= topk_groups <= n_groups and topk_groups * (n_routed / n_groups) >=
+ * top_k (else MOE_ERR_INVALID_ARG; n_groups > 32: MOE_ERR_UNSUPPORTED).
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -71,12 +74,20 @@ typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 
 /* One layer's shape.  T tokens of hidden size H; n_routed routed experts of
  * which top_k are chosen per token; n_shared always-on experts; every expert
- * has intermediate width `inter` (M/m in the segmentation notation). */
+ * has intermediate width `inter` (M/m in the segmentation notation).
+ * n_groups > 0 makes the routing group-limited (page "02 · 细粒度 MoE", §4,
+ * node-limited routing): the routed experts form n_groups groups of
+ * n_routed / n_groups consecutive experts, each token keeps the topk_groups
+ * groups with the largest sum of its experts' scores (softmax scores, or
+ * s + b with MOE_GATE_SIGMOID_BIAS), ties to the lower group index, and
+ * chooses its top_k experts among those groups only.  n_groups = 0 (and
+ * topk_groups = 0): no limit. */
 typedef struct {
   int32_t T, H, n_routed, n_shared, top_k, inter;
   int32_t gate;  /* moe_gate */
   int32_t act;   /* moe_act */
   int32_t dtype; /* moe_dtype */
+  int32_t n_groups, topk_groups;
 } moe_shape;
 
 /* Layer parameters (device pointers).  logit_offset [E] (may be NULL) is

@@ -32,8 +32,12 @@ def bias_np(inp: W.MoEInputs):
 
 
 def oracle_route(shape: W.MoEShape, logits_np, inp: W.MoEInputs):
-    return O.route(logits_np, shape.gate, shape.top_k,
-                   bias_np(inp) if shape.gate == W.GATE_SIGMOID_BIAS else None)
+    r = O.route(logits_np, shape.gate, shape.top_k,
+                bias_np(inp) if shape.gate == W.GATE_SIGMOID_BIAS else None,
+                shape.n_groups, shape.topk_groups)
+    # a near-tie of the last kept group counts like one of the k-th expert
+    r["gap"] = np.minimum(r["gap"], r["group_gap"])
+    return r
 
 
 def gpu_route(shape, logits: torch.Tensor, bias):

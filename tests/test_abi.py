@@ -77,12 +77,25 @@ def test_workspace_sizes_cover_the_buffers():
     (dict(n_routed=64, top_k=33), M.MOE_ERR_UNSUPPORTED),
     (dict(H=200), M.MOE_ERR_UNSUPPORTED),            # bf16 needs H % 128
     (dict(inter=96), M.MOE_ERR_UNSUPPORTED),         # bf16 SwiGLU needs inter % 64
+    # group-limited routing
+    (dict(n_groups=3, topk_groups=1), M.MOE_ERR_INVALID_ARG),   # 16 % 3 != 0
+    (dict(n_groups=4, topk_groups=0), M.MOE_ERR_INVALID_ARG),
+    (dict(n_groups=4, topk_groups=5), M.MOE_ERR_INVALID_ARG),
+    (dict(n_groups=8, topk_groups=1), M.MOE_ERR_INVALID_ARG),   # 1 group of 2 < top_k 4
+    (dict(n_groups=0, topk_groups=2), M.MOE_ERR_INVALID_ARG),
+    (dict(n_groups=-1, topk_groups=1), M.MOE_ERR_INVALID_ARG),
+    (dict(n_routed=64, n_groups=64, topk_groups=8), M.MOE_ERR_UNSUPPORTED),  # > 32 groups
 ])
 def test_bad_shapes_rejected_on_host(bad, code):
     s = _shape(**bad)
     assert M.lib().moe_layer_workspace_size(ctypes.byref(s)) == 0
     st = M.lib().moe_route(ctypes.byref(s), 256, None, 256, 256, None, None)
     assert st == code
+
+
+def test_group_limited_shape_accepted():
+    s = _shape(n_groups=4, topk_groups=2)
+    assert M.lib().moe_layer_workspace_size(ctypes.byref(s)) > 0
 
 
 def test_null_and_misaligned_pointers_rejected():

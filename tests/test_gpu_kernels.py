@@ -63,6 +63,49 @@ def test_route_bit_exact_from_same_logits(E, k, gate, kind):
     assert np.all(np.abs(g[fin] - ref["gap"][fin]) <= 1e-6 + 1e-5 * np.abs(ref["gap"][fin]))
 
 
+GROUP_CASES = [
+    # (E, k, n_groups, topk_groups, gate, kind)
+    (256, 8, 8, 4, W.GATE_SIGMOID_BIAS, "normal"),   # the V3 setting: 8 groups, 4 kept
+    (64, 6, 4, 2, W.GATE_SOFTMAX, "normal"),
+    (64, 8, 8, 2, W.GATE_SIGMOID_BIAS, "skewed"),    # exactly k experts in the kept groups
+    (96, 6, 32, 6, W.GATE_SOFTMAX, "skewed"),        # 32 groups of 3
+    (16, 2, 4, 1, W.GATE_SOFTMAX, "ties"),           # integer logits: exact group ties
+    (40, 5, 5, 5, W.GATE_SIGMOID_BIAS, "normal"),    # every group kept = no limit
+    (384, 8, 32, 4, W.GATE_SIGMOID_BIAS, "normal"),
+]
+
+
+@pytest.mark.parametrize("E,k,G,M,gate,kind", GROUP_CASES)
+def test_group_limited_route_bit_exact_from_same_logits(E, k, G, M, gate, kind):
+    """Group-limited routing (page "02 · 细粒度 MoE", §4): the choice equals the
+    oracle's from the same fp32 logits except where the last kept group or the
+    k-th expert wins by less than 1e-5 (reported, not failed)."""
+    T = 1001
+    shape = S("groups", T=T, n_routed=E, top_k=k, gate=gate, n_groups=G, topk_groups=M)
+    z = W.random_logits(T, E, seed=E * 7 + G, kind=kind)
+    bias = None
+    if gate == W.GATE_SIGMOID_BIAS:
+        g = torch.Generator().manual_seed(E + G)
+        bias = (torch.rand(E, generator=g) * 0.2 - 0.1)
+    ref = O.route(z.numpy(), gate, k, None if bias is None else bias.numpy(), G, M)
+    idx, w, gap = gpu_route(shape, z.to(DEV), None if bias is None else bias.to(DEV))
+    near = dict(ref)
+    near["gap"] = np.minimum(ref["gap"], ref["group_gap"])
+    diff = compare_routing(shape, idx, w, near)
+    gi = idx.cpu().numpy()
+    gsize = E // G
+    # every chosen expert lies in a kept group: at most M distinct groups per token
+    assert max(len(set((gi[t] // gsize).tolist())) for t in range(T)) <= M
+    if kind == "ties":
+        assert not diff.any()     # exact group and expert ties go to the lower index on both sides
+    g = gap.cpu().numpy().astype(np.float64)
+    same = ~diff
+    fin = np.isfinite(ref["gap"]) & same
+    assert np.array_equal(np.isfinite(g)[same], np.isfinite(ref["gap"])[same])
+    assert np.all(np.abs(g[fin] - ref["gap"][fin]) <= 1e-6 + 1e-5 * np.abs(ref["gap"][fin]))
+    print(f"E={E} G={G} M={M}: {int(diff.sum())} near-tie flips")
+
+
 def test_route_zero_tokens_and_zero_k():
     shape = S("empty", T=0, n_routed=8, top_k=2)
     z = torch.empty((0, 8), device=DEV)

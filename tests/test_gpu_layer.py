@@ -76,6 +76,9 @@ SMALL = [
     W.MoEShape("one_token", T=1, H=256, n_routed=8, n_shared=1, top_k=3, inter=64),
     dataclasses.replace(W.SHAPES["tiny_f32"], name="tiny_f32_sigmoid",
                         gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, act=W.ACT_SWIGLU),
+    # group-limited routing, V3-style: 64 experts in 8 groups, 4 groups kept
+    W.MoEShape("small_groups", T=700, H=256, n_routed=64, n_shared=1, top_k=8, inter=128,
+               gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, n_groups=8, topk_groups=4),
 ]
 
 
