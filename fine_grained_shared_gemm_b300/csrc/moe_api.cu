@@ -248,14 +248,34 @@ size_t act_rows(const moe_shape* s) {
   return static_cast<size_t>(s->T) * (s->top_k + s->n_shared);
 }
 
+// Shared experts are planned as pieces of kSharedPiece tokens (a multiple of
+// every token-tile height) spread between the routed experts; the number of
+// pieces keeps the group count within the grouped GEMM's 1024.
+constexpr int kSharedPiece = 512;
+
+int shared_pieces(const moe_shape* s) {
+  if (s->n_shared == 0 || s->T == 0) return 0;
+  const int cap = (1024 - s->n_routed) / s->n_shared;  // >= 1: n_routed + n_shared <= 1024
+  return std::max(1, std::min(cdiv(s->T, kSharedPiece), cap));
+}
+
+int shared_piece_rows(const moe_shape* s) {
+  const int p = shared_pieces(s);
+  return p == 0 ? 0 : cdiv(cdiv(s->T, p), kSharedPiece) * kSharedPiece;
+}
+
+size_t ffn_groups(const moe_shape* s) {
+  return static_cast<size_t>(s->n_routed) + static_cast<size_t>(s->n_shared) * shared_pieces(s);
+}
+
 size_t ffn_ws_bytes(const moe_shape* s) {
-  const size_t G = s->n_routed + s->n_shared;
+  const size_t G = ffn_groups(s);
   return 2 * align256(G * sizeof(GroupDesc)) + align256((G + 1) * 4) +
          align256(act_rows(s) * s->inter * elt_bytes(s));
 }
 
 FfnWs carve_ffn(void* ws, const moe_shape* s) {
-  const size_t G = s->n_routed + s->n_shared;
+  const size_t G = ffn_groups(s);
   char* p = static_cast<char*>(ws);
   FfnWs w;
   w.g1 = reinterpret_cast<GroupDesc*>(p);
@@ -417,14 +437,15 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
                          void* y_shared, void* ws, cudaStream_t st) {
   const int T = s->T, E = s->n_routed, Ks = s->n_shared, k = s->top_k, H = s->H,
             I = s->inter;
-  const int G = E + Ks, Tk = T * k;
+  const int G = static_cast<int>(ffn_groups(s)), Tk = T * k;
   const int rows_act = static_cast<int>(act_rows(s));
   if (T == 0 || rows_act == 0) return MOE_OK;
   FfnWs f = carve_ffn(ws, s);
   const bool f32 = s->dtype == MOE_DTYPE_F32;
   const int bn = f32 ? kSimtTile : ffn_bn(s);
-  ffn_plan_kernel<<<1, cdiv(G, 32) * 32, 0, st>>>(offsets, E, Ks, T, Tk, I, H, bn, f.g1, f.g2,
-                                                   f.tile_prefix);
+  ffn_plan_kernel<<<1, cdiv(G, 32) * 32, 0, st>>>(offsets, E, Ks, T, Tk, I, H, bn,
+                                                   shared_pieces(s), shared_piece_rows(s), f.g1,
+                                                   f.g2, f.tile_prefix);
   MOE_CUDA(cudaGetLastError());
   const bool swiglu = s->act == MOE_ACT_SWIGLU;
 

@@ -95,30 +95,48 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
 }
 
 // Per-group descriptors of the two expert GEMMs and the prefix of token
-// tiles (of `bn` rows) per group.  Groups 0..E-1 are the routed experts on
-// their permuted rows; groups E..E+Ks-1 the shared experts on all T rows.
+// tiles (of `bn` rows) per group.  A group is a routed expert on its permuted
+// rows, or a piece of `piece` consecutive tokens of a shared expert.  The
+// n_pieces pieces of every shared expert are spread evenly between the routed
+// experts (pieces of different shared experts alternate), so that tiles whose
+// weights stream from HBM and tiles that reuse their weights from L2 run side
+// by side all through the launch instead of one kind after the other.
 //   GEMM1 (up/gate):  A = w1/w3 stacks, B source 0 = u_perm, 1 = u; out = act
 //   GEMM2 (down):     A = w2 stacks,    B source 0 = act;              out 0 =
 //                     y_perm, out 1 = y_shared
 // act rows: routed rows first (same row numbers as u_perm), then shared
-// expert j's T rows at T·k + j·T.  One block of up to 1024 threads.
+// expert j's T rows at T·k + j·T.  One thread per group, up to 1024 groups.
 __global__ void __launch_bounds__(1024) ffn_plan_kernel(const int32_t* __restrict__ offsets,
                                                         int E, int Ks, int T, int Tk, int I,
-                                                        int H, int bn, GroupDesc* g1,
-                                                        GroupDesc* g2, int* tile_prefix) {
+                                                        int H, int bn, int n_pieces, int piece,
+                                                        GroupDesc* g1, GroupDesc* g2,
+                                                        int* tile_prefix) {
   __shared__ int warp_tot[32];
-  const int g = threadIdx.x, G = E + Ks;
+  const int S = Ks * n_pieces;  // shared pieces
+  const int g = threadIdx.x, G = E + S;
+  int routed = -1, shared_piece = -1;
+  if (g < G) {
+    const int q = S > 0 ? E / S : 0;  // routed experts before each shared piece
+    const int blk = q + 1;
+    if (S == 0) routed = g;
+    else if (g < S * blk) {
+      if (g % blk < q) routed = (g / blk) * q + g % blk;
+      else shared_piece = g / blk;
+    } else {
+      routed = S * q + (g - S * blk);
+    }
+  }
   int cnt = 0;
-  if (g < E) {
-    const int b = offsets[g];
-    cnt = offsets[g + 1] - b;
-    g1[g] = GroupDesc{0, g * I, 0, b, 0, b, cnt, 0};
-    g2[g] = GroupDesc{0, g * H, 0, b, 0, b, cnt, 0};
-  } else if (g < G) {
-    const int j = g - E;
-    cnt = T;
-    g1[g] = GroupDesc{1, j * I, 1, 0, 0, Tk + j * T, T, 0};
-    g2[g] = GroupDesc{1, j * H, 0, Tk + j * T, 1, j * T, T, 0};
+  if (routed >= 0) {
+    const int b = offsets[routed];
+    cnt = offsets[routed + 1] - b;
+    g1[g] = GroupDesc{0, routed * I, 0, b, 0, b, cnt, 0};
+    g2[g] = GroupDesc{0, routed * H, 0, b, 0, b, cnt, 0};
+  } else if (shared_piece >= 0) {
+    const int j = shared_piece % Ks, p0 = (shared_piece / Ks) * piece;
+    cnt = max(0, min(piece, T - p0));
+    g1[g] = GroupDesc{1, j * I, 1, p0, 0, Tk + j * T + p0, cnt, 0};
+    g2[g] = GroupDesc{1, j * H, 0, Tk + j * T + p0, 1, j * T + p0, cnt, 0};
   }
   const int nt = (cnt + bn - 1) / bn;
   const int lane = g & 31, w = g >> 5;
