@@ -443,9 +443,12 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   FfnWs f = carve_ffn(ws, s);
   const bool f32 = s->dtype == MOE_DTYPE_F32;
   const int bn = f32 ? kSimtTile : ffn_bn(s);
+  // weights read by about two token tiles or fewer stream from HBM: mix
+  // heavily and lightly loaded experts through the launch
+  const int by_load = (!f32 && static_cast<long long>(Tk) <= 2LL * bn * E) ? 1 : 0;
   ffn_plan_kernel<<<1, cdiv(G, 32) * 32, 0, st>>>(offsets, E, Ks, T, Tk, I, H, bn,
-                                                   shared_pieces(s), shared_piece_rows(s), f.g1,
-                                                   f.g2, f.tile_prefix);
+                                                   shared_pieces(s), shared_piece_rows(s),
+                                                   by_load, f.g1, f.g2, f.tile_prefix);
   MOE_CUDA(cudaGetLastError());
   const bool swiglu = s->act == MOE_ACT_SWIGLU;
 

@@ -100,7 +100,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
 // n_pieces pieces of every shared expert are spread evenly between the routed
 // experts (pieces of different shared experts alternate), so that tiles whose
 // weights stream from HBM and tiles that reuse their weights from L2 run side
-// by side all through the launch instead of one kind after the other.
+// by side all through the launch instead of one kind after the other.  For
+// the same reason, with `by_load` (weights read by few token tiles), the
+// routed experts are taken by load, alternately from the most and the least
+// loaded (ranks by row count, ties to the lower index): largest, smallest,
+// second largest, ...
 //   GEMM1 (up/gate):  A = w1/w3 stacks, B source 0 = u_perm, 1 = u; out = act
 //   GEMM2 (down):     A = w2 stacks,    B source 0 = act;              out 0 =
 //                     y_perm, out 1 = y_shared
@@ -109,11 +113,23 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtParams p) {
 __global__ void __launch_bounds__(1024) ffn_plan_kernel(const int32_t* __restrict__ offsets,
                                                         int E, int Ks, int T, int Tk, int I,
                                                         int H, int bn, int n_pieces, int piece,
+                                                        int by_load,
                                                         GroupDesc* g1, GroupDesc* g2,
                                                         int* tile_prefix) {
   __shared__ int warp_tot[32];
+  __shared__ int s_count[1024];
+  __shared__ int s_by_rank[1024];
   const int S = Ks * n_pieces;  // shared pieces
   const int g = threadIdx.x, G = E + S;
+  if (g < E) s_count[g] = offsets[g + 1] - offsets[g];
+  __syncthreads();
+  if (by_load && g < E) {
+    const int c = s_count[g];
+    int rank = 0;
+    for (int j = 0; j < E; ++j) rank += (s_count[j] > c) || (s_count[j] == c && j < g);
+    s_by_rank[rank] = g;
+  }
+  __syncthreads();
   int routed = -1, shared_piece = -1;
   if (g < G) {
     const int q = S > 0 ? E / S : 0;  // routed experts before each shared piece
@@ -128,6 +144,7 @@ __global__ void __launch_bounds__(1024) ffn_plan_kernel(const int32_t* __restric
   }
   int cnt = 0;
   if (routed >= 0) {
+    if (by_load) routed = s_by_rank[(routed & 1) ? E - 1 - (routed >> 1) : (routed >> 1)];
     const int b = offsets[routed];
     cnt = offsets[routed + 1] - b;
     g1[g] = GroupDesc{0, routed * I, 0, b, 0, b, cnt, 0};
