@@ -35,13 +35,25 @@ __global__ void __launch_bounds__(256) combine_kernel(
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] += y[i];
       }
-      for (int s = 0; s < k; ++s) {
-        const int row = s_row[wib][s];
-        const float w = s_w[wib][s];
-        if (row < 0) continue;
-        Vec16<T>::load(y_perm + static_cast<size_t>(row) * H + v * V, y);
+      // routed slots in groups of 8: all loads of a group are issued before
+      // any is used (independent predicated loads), then accumulated in slot
+      // order, so the sum is the same as one slot at a time
+      for (int s0 = 0; s0 < k; s0 += 8) {
+        uint4 raw[8];
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+        for (int d = 0; d < 8; ++d) {
+          const int row = s0 + d < k ? s_row[wib][s0 + d] : -1;
+          raw[d] = row >= 0 ? __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(row) * H + v * V))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          if (s0 + d >= k || s_row[wib][s0 + d] < 0) continue;
+          const float w = s_w[wib][s0 + d];
+          Vec16<T>::load(reinterpret_cast<const T*>(&raw[d]), y);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+        }
       }
       Vec16<T>::store(h + static_cast<size_t>(t) * H + v * V, acc);
     }
