@@ -267,6 +267,40 @@ def update_select_bias(loads: np.ndarray, select_bias: np.ndarray, gamma: float,
     return b.astype(np.float32)
 
 
+def balance_stats(z: np.ndarray, idx: np.ndarray, n_routed: int, top_k: int,
+                  gate: str):
+    """Per-expert statistics of the expert-level balance loss ([PS], load
+    balance section): f_i, the actual routing distribution, and P_i, the
+    gate's mean probability for expert i; the loss is proportional to
+    Σ_i f_i P_i.  The page's formula did not survive extraction; the reading:
+
+      f_i = E · #{(t, s) : idx[t, s] = i} / (k · T)   (the count runs over all
+            E routed experts, so a perfectly even routing gives f_i = 1);
+      P_i = (1/T) Σ_t p_{i,t}, p_t the token's gate distribution over the E
+            routed experts: the softmax scores, or for the sigmoid gate the
+            scores divided by their sum over all E (so Σ_i P_i = 1 for both).
+
+    z are the fp32 logits (logit offset included).  f is returned in float32
+    (one rounding of the exact ratio), P in float64.  k = 0 gives f = 0.
+    """
+    z = np.asarray(z, np.float64)
+    T = z.shape[0]
+    E = n_routed
+    loads = expert_loads(idx, E) if T and top_k else np.zeros(E, np.int64)
+    if T == 0 or top_k == 0:
+        f = np.zeros(E, np.float32)
+    else:
+        f = ((E * loads).astype(np.float64) / float(top_k * T)).astype(np.float32)
+    if T == 0:
+        return f, np.zeros(E, np.float64)
+    if gate == SOFTMAX:
+        p = softmax_scores(z)
+    else:
+        s = sigmoid_scores(z)
+        p = s / s.sum(axis=1, keepdims=True)
+    return f, p.sum(axis=0) / T
+
+
 # --------------------------------------------------------------------------
 # Expert FFN and combine ([PS]; [FG] Eq. 9–11)
 # --------------------------------------------------------------------------

@@ -352,14 +352,62 @@ def check_group_routing_bruteforce(o):
             assert np.array_equal(np.sort(one["idx"], 1), np.sort(plain["idx"], 1))
 
 
+def _exact(v):
+    """'ln3' -> log(3), '4/3' -> 4/3, '0' -> 0 (values of the hand-worked fixtures)."""
+    if v.startswith("ln"):
+        return math.log(float(v[2:]))
+    num, _, den = v.partition("/")
+    return float(num) / float(den or 1)
+
+
+def check_balance_stats_handworked(o, golden_dir):
+    for c in _load(golden_dir, "balance_stats_handworked.json")["cases"]:
+        z = np.array([[_exact(v) for v in row] for row in c["logits"]], np.float32)
+        idx = np.array(c["idx"])
+        r = o.route(z, c["gate"], c["top_k"])
+        assert np.array_equal(r["idx"], idx), (c, r["idx"])
+        f, p = o.balance_stats(z, idx, z.shape[1], c["top_k"], c["gate"])
+        assert f.dtype == np.float32
+        assert np.array_equal(f, np.array([_exact(v) for v in c["f"]], np.float32)), (c, f)
+        assert np.allclose(p, [_exact(v) for v in c["P"]], rtol=0, atol=1e-7), (c, p)
+
+
+def check_balance_stats_properties(o):
+    """Σ f_i = E and Σ P_i = 1 on random routings; an even routing gives
+    f_i = 1; f depends on the choice only, P on the logits only; when every
+    expert is chosen (k = E) P_i is the token mean of the gate weights the
+    router gives expert i (no renormalisation under softmax, normalisation
+    over all E under sigmoid)."""
+    rng = np.random.default_rng(11)
+    T, E, k = 96, 8, 3
+    for gate in (o.SOFTMAX, o.SIGMOID_BIAS):
+        z = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+        r = o.route(z, gate, k)
+        f, p = o.balance_stats(z, r["idx"], E, k, gate)
+        assert abs(float(f.astype(np.float64).sum()) - E) < 1e-5
+        assert abs(p.sum() - 1.0) < 1e-12
+        even = np.array([[(t + j) % E for j in range(k)] for t in range(T)])
+        f_even, p2 = o.balance_stats(z, even, E, k, gate)
+        assert np.array_equal(f_even, np.ones(E, np.float32))
+        assert np.array_equal(p2, p)
+        f3, _ = o.balance_stats(z[::-1] * 0.5, r["idx"], E, k, gate)
+        assert np.array_equal(f3, f)
+        full = o.route(z, gate, E)
+        w = np.zeros((T, E))
+        np.put_along_axis(w, full["idx"], full["weights"], axis=1)
+        _, p_full = o.balance_stats(z, full["idx"], E, E, gate)
+        assert np.allclose(p_full, w.mean(axis=0), rtol=1e-12, atol=1e-15)
+
+
 CHECKS = [check_routing_handworked, check_ffn_handworked, check_combinations,
-          check_bias_update_handworked, check_group_routing_handworked]
+          check_bias_update_handworked, check_group_routing_handworked,
+          check_balance_stats_handworked]
 PLAIN_CHECKS = [check_topk_bruteforce, check_softmax_properties,
                 check_softmax_choice_is_score_order, check_sigmoid_properties,
                 check_segmentation_identity, check_ffn_bruteforce,
                 check_classic_moe, check_shared_equals_forced_routed,
                 check_combine_zero_gates, check_dispatch, check_bias_controller_balances,
-                check_group_routing_bruteforce]
+                check_group_routing_bruteforce, check_balance_stats_properties]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -463,7 +511,21 @@ def test_planted_mistakes(golden_dir):
         np.put_along_axis(allowed, gidx, True, axis=1)
         return np.repeat(allowed, E // n_groups, axis=1), np.full(T, np.inf)
 
+    def f_over_tokens(z, idx, n_routed, top_k, gate):
+        f, p = O.balance_stats(z, idx, n_routed, top_k, gate)
+        return (f * np.float32(top_k) / np.float32(n_routed)).astype(np.float32), p
+
+    def sigmoid_unnormalised(z, idx, n_routed, top_k, gate):
+        f, p = O.balance_stats(z, idx, n_routed, top_k, gate)
+        if gate != O.SOFTMAX:
+            p = O.sigmoid_scores(z).mean(axis=0)
+        return f, p
+
     cases = [
+        (dict(balance_stats=f_over_tokens), check_balance_stats_handworked, (golden_dir,)),
+        (dict(balance_stats=f_over_tokens), check_balance_stats_properties, ()),
+        (dict(balance_stats=sigmoid_unnormalised), check_balance_stats_handworked, (golden_dir,)),
+        (dict(balance_stats=sigmoid_unnormalised), check_balance_stats_properties, ()),
         (dict(group_choice=group_by_max), check_group_routing_handworked, (golden_dir,)),
         (dict(group_choice=group_by_max), check_group_routing_bruteforce, ()),
         (dict(update_select_bias=bias_sign_flipped), check_bias_update_handworked, (golden_dir,)),
