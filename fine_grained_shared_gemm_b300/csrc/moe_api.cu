@@ -763,6 +763,31 @@ MOE_API moe_status moe_update_select_bias(const moe_shape* s, const int32_t* exp
   return MOE_OK;
 }
 
+MOE_API size_t moe_balance_stats_workspace_size(const moe_shape* s) {
+  if (check_shape(s) != MOE_OK) return 0;
+  return align256(static_cast<size_t>(cdiv(s->T, kStatChunk)) * s->n_routed * sizeof(float));
+}
+
+MOE_API moe_status moe_balance_stats(const moe_shape* s, const float* logits,
+                                     const int32_t* expert_offsets, float* f, float* p, void* ws,
+                                     size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (!ok_ptr(expert_offsets) || !ok_ptr(f) || !ok_ptr(p)) return MOE_ERR_INVALID_ARG;
+  if (s->T > 0 && !ok_ptr(logits)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_balance_stats_workspace_size(s);
+  if (need > 0 && (ws == nullptr || !al16(ws) || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  const int E = s->n_routed;
+  const int n_chunks = cdiv(s->T, kStatChunk);
+  float* partial = static_cast<float*>(ws);
+  if (n_chunks > 0)
+    balance_partial_kernel<<<n_chunks, 256, 0, cs(stream)>>>(
+        logits, s->T, E, s->gate == MOE_GATE_SIGMOID_BIAS, partial);
+  balance_final_kernel<<<cdiv(E, 256), 256, 0, cs(stream)>>>(partial, n_chunks, expert_offsets,
+                                                             s->T, E, s->top_k, f, p);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_layer_forward(const moe_shape* s, const moe_weights* weights,
                                      const void* u, void* h, const moe_route_outputs* route_out,
                                      void* ws, size_t ws_bytes, moe_stream_t stream) {

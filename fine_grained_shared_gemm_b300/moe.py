@@ -74,6 +74,8 @@ _SIGNATURES = {
     "moe_layer_forward_host": (ctypes.c_int, [_S, _W, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch_static": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P]),
     "moe_update_select_bias": (ctypes.c_int, [_S, _P, _P, ctypes.c_float, _P, _P]),
+    "moe_balance_stats_workspace_size": (ctypes.c_size_t, [_S]),
+    "moe_balance_stats": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -148,6 +150,10 @@ def moe_layer_workspace_size(shape) -> int:
     return lib().moe_layer_workspace_size(ctypes.byref(shape_struct(shape)))
 
 
+def moe_balance_stats_workspace_size(shape) -> int:
+    return lib().moe_balance_stats_workspace_size(ctypes.byref(shape_struct(shape)))
+
+
 def moe_device_status(stream=None):
     """(status, raw device error word); synchronises the stream."""
     code = ctypes.c_int32(0)
@@ -190,6 +196,13 @@ def moe_update_select_bias(shape, expert_offsets, select_bias, gamma: float, loa
     _check("moe_update_select_bias", lib().moe_update_select_bias(
         ctypes.byref(shape_struct(shape)), _ptr(expert_offsets), _ptr(select_bias),
         ctypes.c_float(gamma), _ptr(loads), _stream(stream)))
+
+
+def moe_balance_stats(shape, logits, expert_offsets, f, p, ws, stream=None):
+    """f_i and P_i of the expert-level balance loss into f, p [E] fp32."""
+    _check("moe_balance_stats", lib().moe_balance_stats(
+        ctypes.byref(shape_struct(shape)), _ptr(logits), _ptr(expert_offsets), _ptr(f), _ptr(p),
+        _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_expert_ffn(shape, weights: moe_weights, u, u_perm, expert_offsets, y_perm, y_shared,

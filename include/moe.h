@@ -199,6 +199,27 @@ MOE_API moe_status moe_update_select_bias(const moe_shape* shape,
                                           float* select_bias, float gamma,
                                           int32_t* loads, moe_stream_t stream);
 
+/* Statistics of the expert-level balance loss (page "19-deepseek-moe",
+ * ai.tomabc.com, load-balance section: the loss is proportional to
+ * Σ_i f_i P_i).  That formula did not survive on the page; the reading:
+ *   f[i] = E · L_i / (k · T), L_i = expert_offsets[i+1] - expert_offsets[i],
+ *          the routing distribution counted over all E routed experts (an
+ *          even routing gives 1); one fp64 division, rounded to fp32; 0 when
+ *          k · T = 0;
+ *   p[i] = (1/T) Σ_t q_{i,t}, q_t the token's gate distribution over the E
+ *          routed experts computed from logits [T, E] (fp32, as
+ *          moe_router_logits writes them): softmax scores, or for
+ *          MOE_GATE_SIGMOID_BIAS the sigmoid scores divided by their sum over
+ *          all E (select_bias plays no part); 0 when T = 0.
+ * f, p [E] fp32 out.  The sums run in a fixed order (fp32 within 256-token
+ * chunks, fp64 across chunks), so results are reproducible.  Group limits
+ * in the shape are ignored.  ws: moe_balance_stats_workspace_size bytes. */
+MOE_API size_t moe_balance_stats_workspace_size(const moe_shape* shape);
+MOE_API moe_status moe_balance_stats(const moe_shape* shape, const float* logits,
+                                     const int32_t* expert_offsets, float* f,
+                                     float* p, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
 /* Whole layer: router logits, route, dispatch, expert FFNs, combine, all on
  * `stream`.  route_out (may be NULL) receives copies of the routing
  * intermediates.  ws: moe_layer_workspace_size bytes. */

@@ -135,3 +135,21 @@ def test_bias_update_rejects_bad_gamma_and_pointers():
         M.MOE_ERR_INVALID_ARG
     assert L.moe_update_select_bias(ctypes.byref(s), 256, 258, f(0.1), None, None) == \
         M.MOE_ERR_INVALID_ARG
+
+
+def test_balance_stats_rejects_bad_pointers_and_workspace():
+    s = _shape()
+    L = M.lib()
+    need = L.moe_balance_stats_workspace_size(ctypes.byref(s))
+    assert need >= s.n_routed * 4 * ((s.T + 255) // 256) and need % 256 == 0
+    args = [256, 256, 256, 256, 256, need, None]
+    for i in range(4):   # logits, offsets, f, p
+        bad = list(args)
+        bad[i] = None
+        assert L.moe_balance_stats(ctypes.byref(s), *bad) == M.MOE_ERR_INVALID_ARG, i
+        bad[i] = 258
+        assert L.moe_balance_stats(ctypes.byref(s), *bad) == M.MOE_ERR_INVALID_ARG, i
+    assert L.moe_balance_stats(ctypes.byref(s), 256, 256, 256, 256, 256, need - 1, None) == \
+        M.MOE_ERR_WORKSPACE
+    assert L.moe_balance_stats(ctypes.byref(s), 256, 256, 256, 256, None, need, None) == \
+        M.MOE_ERR_WORKSPACE

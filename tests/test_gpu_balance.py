@@ -75,3 +75,47 @@ def test_bias_controller_closed_loop_on_gpu():
     assert M.moe_device_status()[0] == M.MOE_OK
     assert imbalance[0] > 1.6, imbalance[0]
     assert max(imbalance[-20:]) < 1.12, imbalance[-20:]
+
+
+@pytest.mark.parametrize("gate", [W.GATE_SOFTMAX, W.GATE_SIGMOID_BIAS])
+@pytest.mark.parametrize("T,E,k", [(1, 4, 2), (255, 64, 6), (1000, 257, 8), (4097, 16, 3)])
+def test_balance_stats_against_oracle(gate, T, E, k):
+    """f_i and P_i of the expert-level balance loss (page "19-deepseek-moe",
+    load-balance section) from the kernels' own logits, routing and dispatch:
+    f bit-exact (an exact integer ratio rounded once), P within 1e-5 of its
+    largest entry (fp32 scores and sums of at most 256 terms; the oracle sums
+    float64 scores)."""
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(T * 7 + E)
+    H = 128
+    u = torch.randn((T, H), generator=gen, device=DEV).to(torch.bfloat16)
+    cents = (torch.randn((E, H), generator=gen, device=DEV) / H ** 0.5 * 3).to(torch.bfloat16)
+    shape = W.MoEShape("stats", T=T, H=H, n_routed=E, n_shared=0, top_k=k, inter=64, gate=gate)
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    M.moe_router_logits(shape, u, cents, None, logits)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    M.moe_route(shape, logits, None, idx, w)
+    off = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    row_token = torch.empty((T * k,), dtype=torch.int32, device=DEV)
+    slot_row = torch.empty((T * k,), dtype=torch.int32, device=DEV)
+    u_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=DEV)
+    M.moe_dispatch(shape, idx, u, off, row_token, slot_row, u_perm,
+                   M.alloc_workspace(M.moe_dispatch_workspace_size(shape), DEV))
+    f = torch.full((E,), float("nan"), dtype=torch.float32, device=DEV)
+    p = torch.full((E,), float("nan"), dtype=torch.float32, device=DEV)
+    ws = M.alloc_workspace(M.moe_balance_stats_workspace_size(shape), DEV)
+    M.moe_balance_stats(shape, logits, off, f, p, ws)
+    torch.cuda.synchronize()
+    assert M.moe_device_status()[0] == M.MOE_OK
+    want_f, want_p = O.balance_stats(logits.cpu().numpy(), idx.cpu().numpy(), E, k,
+                                     O.SOFTMAX if gate == W.GATE_SOFTMAX else O.SIGMOID_BIAS)
+    assert np.array_equal(f.cpu().numpy(), want_f)
+    got_p = p.cpu().numpy().astype(np.float64)
+    assert np.abs(got_p - want_p).max() <= 1e-5 * want_p.max(), np.abs(got_p - want_p).max()
+    assert abs(got_p.sum() - 1.0) < 1e-4
+    # a second call gives the same bits (fixed-order sums)
+    p2 = torch.empty_like(p)
+    M.moe_balance_stats(shape, logits, off, f, p2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(p, p2)
