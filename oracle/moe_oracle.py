@@ -1,4 +1,4 @@
-"""CPU oracle for the DeepSeekMoE layer forward.
+"""CPU oracle for the DeepSeekMoE layer forward and its backward.
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 benchmark's CPU-baseline leg may import this module.  The product path (the
@@ -370,6 +370,137 @@ def layer_forward(u: np.ndarray, route_out: dict, routed: ExpertFn,
         w1, w3, w2 = routed(int(e))
         y_r[tt, ss] = expert_ffn(x[tt], w1, w2, w3, act)
     return combine(x, y_sh, y_r, g)
+
+
+# --------------------------------------------------------------------------
+# Backward of the layer (training side of [FG] Eq. 9–15 and [PS])
+# --------------------------------------------------------------------------
+# The choice of experts is piecewise constant in the logits, so gradients
+# flow through the gate weights, the expert FFNs and the residual, with the
+# chosen set held fixed; the selection bias (choice only) gets none.
+
+def gate_weights(z: np.ndarray, idx: np.ndarray, gate: str):
+    """Gate weights of the chosen experts as a function of float64 logits.
+
+    softmax: g = s_i for the chosen i, s = softmax over the E routed logits
+    ([FG] Eq. 6–8, no renormalisation); sigmoid: g = s_i / Σ_chosen s_j,
+    s = sigmoid(z) ([FG] Eq. 12–15).  Returns (g [T,k], s [T,E]).
+    """
+    z = np.asarray(z, np.float64)
+    s = softmax_scores(z) if gate == SOFTMAX else sigmoid_scores(z)
+    idx = np.asarray(idx, np.int64)
+    g = np.take_along_axis(s, idx, axis=1)
+    if gate == SIGMOID_BIAS and idx.shape[1] > 0:
+        g = g / g.sum(axis=1, keepdims=True)
+    return g, s
+
+
+def gate_backward(z: np.ndarray, idx: np.ndarray, gate: str, dg: np.ndarray) -> np.ndarray:
+    """dL/dz [T,E] from dL/dg [T,k] for the fixed choice idx.
+
+    softmax: ∂s_i/∂z_j = s_i (δ_ij − s_j), so dz_j = s_j (dg_j [j chosen]
+    − Σ_chosen dg_i s_i).  sigmoid: ∂g_i/∂s_j = (δ_ij − g_i) / S for chosen
+    j (S = Σ_chosen s), ds/dz = s (1 − s), unchosen experts get 0.
+    """
+    g, s = gate_weights(z, idx, gate)
+    idx = np.asarray(idx, np.int64)
+    dg = np.asarray(dg, np.float64)
+    T, E = s.shape
+    dz = np.zeros((T, E))
+    if idx.shape[1] == 0:
+        return dz
+    if gate == SOFTMAX:
+        ds = np.zeros((T, E))
+        np.put_along_axis(ds, idx, dg, axis=1)
+        dz = s * (ds - (ds * s).sum(axis=1, keepdims=True))
+    else:
+        sc = np.take_along_axis(s, idx, axis=1)
+        S = sc.sum(axis=1, keepdims=True)
+        ds_sel = (dg - (dg * g).sum(axis=1, keepdims=True)) / S
+        np.put_along_axis(dz, idx, ds_sel * sc * (1.0 - sc), axis=1)
+    return dz
+
+
+def expert_ffn_backward(x: np.ndarray, w1: np.ndarray, w2: np.ndarray,
+                        w3: Optional[np.ndarray], act: str, dy: np.ndarray):
+    """Gradients of y = expert_ffn(x) for the upstream dL/dy, float64.
+
+    With a = x W1ᵀ, c = x W3ᵀ and m = ReLU(a) or SiLU(a) ⊙ c (y = m W2ᵀ):
+    dm = dy W2; relu: da = dm ⊙ [a > 0]; swiglu: da = dm ⊙ c ⊙ SiLU'(a),
+    dc = dm ⊙ SiLU(a), SiLU'(a) = σ(a) (1 + a (1 − σ(a))).
+    Returns (dx, dw1, dw3 or None, dw2) with dw1 = daᵀ x, dw3 = dcᵀ x,
+    dw2 = dyᵀ m, dx = da W1 + dc W3.
+    """
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    w1 = np.asarray(w1, np.float64)
+    w2 = np.asarray(w2, np.float64)
+    a = x @ w1.T
+    dm = dy @ w2
+    if act == RELU:
+        m = np.maximum(a, 0.0)
+        da = dm * (a > 0)
+        return da @ w1, da.T @ x, None, dy.T @ m
+    if act != SWIGLU:
+        raise ValueError(act)
+    w3 = np.asarray(w3, np.float64)
+    c = x @ w3.T
+    sg = 1.0 / (1.0 + np.exp(-a))
+    m = a * sg * c
+    da = dm * c * sg * (1.0 + a * (1.0 - sg))
+    dc = dm * a * sg
+    return da @ w1 + dc @ w3, da.T @ x, dc.T @ x, dy.T @ m
+
+
+def layer_backward(u: np.ndarray, dh: np.ndarray, centroids: np.ndarray,
+                   z: np.ndarray, idx: np.ndarray, gate: str, routed: ExpertFn,
+                   shared: ExpertFn, n_routed: int, n_shared: int, act: str):
+    """Gradients of L = Σ dh ⊙ h (h from :func:`layer_forward` with the gate
+    weights of :func:`gate_weights`) for the fixed choice idx, float64.
+
+    h_t = u_t + Σ_j FFN_j^sh(u_t) + Σ_s g_{t,s} FFN_{idx[t,s]}(u_t) and
+    z_t = centroids u_t (+ offset), so
+      du_t = dh_t + Σ_j J_j^T dh_t + Σ_s g_{t,s} J_{idx[t,s]}^T dh_t + Σ_i dz_{t,i} e_i,
+      dg_{t,s} = <dh_t, FFN_{idx[t,s]}(u_t)>,  d e_i = Σ_t dz_{t,i} u_t.
+    Returns dict(du, d_centroids, dg, dz, dw1, dw3, dw2 [E, ...] and the
+    shared dsw1, dsw3, dsw2 [Ks, ...]); experts nobody chose get zeros;
+    dw3 / dsw3 are None for ReLU.
+    """
+    u = np.asarray(u, np.float64)
+    dh = np.asarray(dh, np.float64)
+    idx = np.asarray(idx, np.int64)
+    T, H = u.shape
+    k = idx.shape[1]
+    g, _ = gate_weights(z, idx, gate)
+    du = dh.copy()
+    out = dict(dsw1=[], dsw3=[], dsw2=[])
+    for j in range(n_shared):
+        w1, w3, w2 = shared(j)
+        dx, dw1, dw3, dw2 = expert_ffn_backward(u, w1, w2, w3, act, dh)
+        du += dx
+        out["dsw1"].append(dw1)
+        out["dsw3"].append(dw3)
+        out["dsw2"].append(dw2)
+    dg = np.zeros((T, k))
+    dw1s, dw3s, dw2s = [None] * n_routed, [None] * n_routed, [None] * n_routed
+    for e in range(n_routed):
+        w1, w3, w2 = routed(e)
+        tt, ss = np.nonzero(idx == e)
+        x = u[tt]
+        dg[tt, ss] = (dh[tt] * expert_ffn(x, w1, w2, w3, act)).sum(axis=1)
+        dy = g[tt, ss][:, None] * dh[tt]
+        dx, dw1s[e], dw3s[e], dw2s[e] = expert_ffn_backward(x, w1, w2, w3, act, dy)
+        du[tt] += dx            # a token picks an expert at most once
+    dz = gate_backward(z, idx, gate, dg)
+    cents = np.asarray(centroids, np.float64)
+    du += dz @ cents
+    out.update(du=du, d_centroids=dz.T @ u, dg=dg, dz=dz,
+               dw1=np.stack(dw1s), dw2=np.stack(dw2s),
+               dw3=None if act == RELU else np.stack(dw3s))
+    for key in ("dsw1", "dsw2", "dsw3"):
+        vals = out[key]
+        out[key] = None if (not vals or vals[0] is None) else np.stack(vals)
+    return out
 
 
 def layer_flops(T: int, H: int, inter: int, top_k: int, n_shared: int,
