@@ -1,0 +1,418 @@
+// Kernels of the layer backward (bf16 layers).  The layer is
+//   h_t = u_t + Σ_j FFN_j^shared(u_t) + Σ_s g_{t,s} FFN_{idx[t,s]}(u_t)
+// (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE", §3.1 Eq. 9–15; expert FFN
+// as on page "19-deepseek-moe"), differentiated with the chosen experts held
+// fixed: the top-k choice is piecewise constant in the logits and the
+// selection bias only changes the choice, so neither passes a gradient.
+//
+// The tensor-core grouped GEMM does the contractions (both operands K-major);
+// the kernels here produce its operands and consume its outputs:
+//   transpose_kernel       weights and token rows into K-major operands (the
+//                          weight gradients contract over each expert's own
+//                          token rows, padded per expert to kSegAlign zeros)
+//   act_backward_kernel    SwiGLU / ReLU derivative per row, the gate-scaled
+//                          activation for dW2 and the per-row <dy, y> for the
+//                          gate gradient
+//   gate_backward_kernel   dL/dz from dL/dg through softmax or the normalised
+//                          sigmoid
+//   router_grad_kernel     dz · centroids and dzᵀ · u (fp32, CUDA cores)
+//   grad_combine_kernel    du = dh + Σ shared dx + Σ slot dx + router term
+//   wgrad_plan_kernel      padded per-expert segments and the weight-gradient
+//                          GEMMs' groups
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "route.cuh"
+
+namespace moe {
+
+// Each expert's token rows start on a multiple of this in the K-major
+// (transposed) operands of the weight-gradient GEMMs: one pipeline stage of
+// the grouped GEMM (two 64-element k-blocks).
+constexpr int kSegAlign = 128;
+
+// ---------------------------------------------------------------- transposes
+
+// dst[c][col0 + j] = src[row(j)][c] for 64 x 64 tiles through shared memory.
+// Two layouts of the j -> row map:
+//   seg_start == nullptr, rows_total >= 0: row(j) = j, columns j >= rows_total
+//     (up to the grid's width) are written as zeros;
+//   seg_start != nullptr: the columns are per-expert segments: expert e owns
+//     [seg_start[e], seg_start[e+1]) and row(j) = offsets[e] + j - seg_start[e]
+//     while that is below offsets[e+1], zeros after; tiles at or past
+//     seg_start[E] write nothing.
+// blockIdx.z selects a matrix of a batch (src/dst advance by their strides).
+// cols (the features, dst rows) % 64 == 0; dst_ld, col0 and the strides are
+// multiples of 8 elements.
+__global__ void __launch_bounds__(256) transpose_kernel(
+    const __nv_bfloat16* __restrict__ src, int src_ld, long long src_bstride, int cols,
+    int rows_total, const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets,
+    int E, __nv_bfloat16* __restrict__ dst, long long dst_ld, long long col0,
+    long long dst_bstride) {
+  __shared__ uint16_t tile[64][66];
+  const int j0 = blockIdx.x * 64;   // first dst column (relative to col0)
+  const int c0 = blockIdx.y * 64;   // first feature
+  src += blockIdx.z * src_bstride;
+  dst += blockIdx.z * dst_bstride;
+  int row0, valid;                  // source row of column j0, valid columns of the tile
+  if (seg_start == nullptr) {
+    row0 = j0;
+    valid = max(0, min(64, rows_total - j0));
+  } else {
+    if (j0 >= seg_start[E]) return;
+    int lo = 0, hi = E;             // largest e with seg_start[e] <= j0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seg_start[mid] <= j0) lo = mid; else hi = mid;
+    }
+    const int local = j0 - seg_start[lo];
+    row0 = offsets[lo] + local;
+    valid = max(0, min(64, offsets[lo + 1] - offsets[lo] - local));
+  }
+  // load: 64 source rows x 64 features, 16 bytes per thread and step
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int r = i >> 3, v = i & 7;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r < valid)
+      x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row0 + r) * src_ld +
+                                               c0 + v * 8));
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(&x);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tile[r][v * 8 + q] = h[q];
+  }
+  __syncthreads();
+  // store: 64 features x 64 columns, 16 bytes per thread and step
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int c = i >> 3, v = i & 7;
+    uint4 x;
+    uint16_t* h = reinterpret_cast<uint16_t*>(&x);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = tile[v * 8 + q][c];
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c0 + c) * dst_ld + col0 + j0 + v * 8) = x;
+  }
+}
+
+// ---------------------------------------------------------------- per-row derivative
+
+// Row r of the expert inputs (routed rows [0, Tk), then shared rows): with
+// a = x W1ᵀ, c = x W3ᵀ (SwiGLU) and dm = dh W2 for the row's token (the
+// upstream gradient NOT yet scaled by the gate weight g of the row; g = 1 for
+// shared rows):
+//   dg_row[r] = <dm, act>           act = SiLU(a) ⊙ c, or ReLU(a)   (r < Tk)
+//   dh1[r]    = [g dm ⊙ c ⊙ SiLU'(a) | g dm ⊙ SiLU(a)]   (SwiGLU, 2I wide)
+//             = g dm ⊙ [a > 0]                            (ReLU, I wide)
+//   actg[r]   = g act
+// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One warp per row, fp32 arithmetic on
+// the bf16 inputs; <dm, act> summed in a fixed order.
+template <bool SWIGLU>
+__global__ void __launch_bounds__(256) act_backward_kernel(
+    const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ c,
+    const __nv_bfloat16* __restrict__ dm, const float* __restrict__ row_gate, long long rows,
+    long long Tk, int I, __nv_bfloat16* __restrict__ dh1, __nv_bfloat16* __restrict__ actg,
+    float* __restrict__ dg_row) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int nvec = I / 8;
+  const int ld1 = SWIGLU ? 2 * I : I;
+  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       r < rows; r += warps) {
+    const float g = r < Tk ? __ldg(row_gate + r) : 1.0f;
+    float dot = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      const size_t off = static_cast<size_t>(r) * I + v * 8;
+      float fa[8], fc[8], fd[8];
+      Vec16<__nv_bfloat16>::load(a + off, fa);
+      Vec16<__nv_bfloat16>::load(dm + off, fd);
+      if (SWIGLU) Vec16<__nv_bfloat16>::load(c + off, fc);
+      float o1[8], o2[8], o3[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (SWIGLU) {
+          const float sg = 1.0f / (1.0f + expf(-fa[i]));
+          const float si = fa[i] * sg;
+          const float act = si * fc[i];
+          dot = fmaf(fd[i], act, dot);
+          const float gd = g * fd[i];
+          o1[i] = gd * fc[i] * sg * (1.0f + fa[i] * (1.0f - sg));
+          o2[i] = gd * si;
+          o3[i] = g * act;
+        } else {
+          const float act = fmaxf(fa[i], 0.0f);
+          dot = fmaf(fd[i], act, dot);
+          o1[i] = fa[i] > 0.0f ? g * fd[i] : 0.0f;
+          o2[i] = 0.0f;
+          o3[i] = g * act;
+        }
+      }
+      const size_t off1 = static_cast<size_t>(r) * ld1 + v * 8;
+      Vec16<__nv_bfloat16>::store(dh1 + off1, o1);
+      if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1 + off1 + I, o2);
+      Vec16<__nv_bfloat16>::store(actg + off, o3);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0 && r < Tk) dg_row[r] = dot;
+  }
+}
+
+// row_gate[slot_row[i]] = topk_w[i]: the gate weight of each permuted row.
+__global__ void __launch_bounds__(256) row_gate_kernel(const int32_t* __restrict__ slot_row,
+                                                       const float* __restrict__ topk_w, int n,
+                                                       float* __restrict__ row_gate) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int r = slot_row[i];
+  if (r >= 0 && r < n) row_gate[r] = topk_w[i];
+}
+
+// ---------------------------------------------------------------- gate
+
+// dL/dz for one token per warp from dg[t, s] = dg_row[slot_row[t, s]]:
+//   softmax (g = s for the chosen): dz_e = s_e (dg_e [e chosen] − Σ_s dg_s g_s)
+//   sigmoid (g = s / S over the chosen): dz_e = (dg_e − Σ_s dg_s g_s) / S ·
+//            s_e (1 − s_e) for chosen e, 0 otherwise.
+// The scores are recomputed from the logits as the router computes them; g
+// is the router's output.  NPL logits per lane (expert e = lane + 32 i).
+template <int NPL>
+__global__ void __launch_bounds__(256) gate_backward_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ slot_row,
+    const float* __restrict__ dg_row, int T, int E, int k, int gate, float* __restrict__ dz) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const float* z = logits + static_cast<size_t>(t) * E;
+    // slot lane < k: its expert, weight and gradient
+    int my_e = -1;
+    float my_g = 0.0f, my_dg = 0.0f, my_s = 0.0f;
+    if (lane < k) {
+      const size_t i = static_cast<size_t>(t) * k + lane;
+      my_e = idx[i];
+      my_g = topk_w[i];
+      my_dg = dg_row[slot_row[i]];
+      if (gate != 0) my_s = 1.0f / (1.0f + expf(-__ldg(z + my_e)));
+    }
+    const float cdot = warp_sum(my_dg * my_g);   // Σ_s dg_s g_s
+    float out[NPL];
+    if (gate == 0) {
+      float key[NPL];
+      float m = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? __ldg(z + e) : -CUDART_INF_F;
+        m = fmaxf(m, key[i]);
+      }
+      m = warp_max(m);
+      float part = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        out[i] = (lane + 32 * i < E) ? expf(key[i] - m) : 0.0f;
+        part += out[i];
+      }
+      const float denom = warp_sum(part);
+      float ds[NPL];
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) ds[i] = 0.0f;
+      for (int s = 0; s < k; ++s) {
+        const int e = __shfl_sync(0xffffffffu, my_e, s);
+        const float d = __shfl_sync(0xffffffffu, my_dg, s);
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (e == lane + 32 * i) ds[i] = d;
+      }
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) out[i] = (out[i] / denom) * (ds[i] - cdot);
+    } else {
+      const float S = warp_sum(my_s);
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) out[i] = 0.0f;
+      for (int s = 0; s < k; ++s) {
+        const int e = __shfl_sync(0xffffffffu, my_e, s);
+        const float d = __shfl_sync(0xffffffffu, my_dg, s);
+        const float sc = __shfl_sync(0xffffffffu, my_s, s);
+        const float v = (d - cdot) / S * (sc * (1.0f - sc));
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (e == lane + 32 * i) out[i] = v;
+      }
+    }
+    float* o = dz + static_cast<size_t>(t) * E;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) o[e] = out[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- router GEMMs
+
+// out[m, n] = Σ_k A(m, k) · B[k, n] in fp32, k ascending: A fp32 with
+// element (m, k) at a[m * sam + k * sak], B bf16 [K, N] row-major, out fp32
+// [M, N] row-major.  64 x 64 output tiles, 4 x 4 per thread, K in steps of 16.
+// Used for dz · centroids (A = dz, sam = E, sak = 1) and dzᵀ · u (sam = 1,
+// sak = E).
+__global__ void __launch_bounds__(256) router_grad_kernel(const float* __restrict__ a,
+                                                          long long sam, long long sak,
+                                                          const __nv_bfloat16* __restrict__ b,
+                                                          int M, int N, int K,
+                                                          float* __restrict__ out) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+      const int kk = i >> 6, mm = i & 63;   // A: consecutive threads along m
+      const int m = m0 + mm, kx = k0 + kk;
+      As[kk][mm] = (m < M && kx < K) ? __ldg(a + m * sam + kx * sak) : 0.0f;
+      const int nn = i & 63;
+      const int n = n0 + nn;
+      Bs[kk][nn] = (n < N && kx < K) ? __bfloat162float(b[static_cast<size_t>(kx) * N + n]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < N) out[static_cast<size_t>(m) * N + n] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- du
+
+// du_t = dh_t + Σ_{j<Ks} dx_shared[j, t] + Σ_{s<k} dx_perm[slot_row[t, s]] + du_router_t,
+// fp32 in this order, one rounding to bf16.  The routed rows were computed
+// from gate-scaled upstream gradients, so they add with weight 1.
+__global__ void __launch_bounds__(256) grad_combine_kernel(
+    const __nv_bfloat16* __restrict__ dh, const __nv_bfloat16* __restrict__ dx_perm,
+    const __nv_bfloat16* __restrict__ dx_shared, const int32_t* __restrict__ slot_row,
+    const float* __restrict__ du_router, int n_tokens, int H, int k, int Ks,
+    __nv_bfloat16* __restrict__ du) {
+  using V16 = Vec16<__nv_bfloat16>;
+  constexpr int V = V16::N;
+  __shared__ int s_row[8][32];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = H / V;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += warps) {
+    __syncwarp();
+    if (lane < k) s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
+    __syncwarp();
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[V], y[V];
+      V16::load(dh + static_cast<size_t>(t) * H + v * V, acc);
+      for (int j = 0; j < Ks; ++j) {
+        V16::load(dx_shared + (static_cast<size_t>(j) * n_tokens + t) * H + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += y[i];
+      }
+      for (int s = 0; s < k; ++s) {
+        const int row = s_row[wib][s];
+        if (row < 0) continue;
+        V16::load(dx_perm + static_cast<size_t>(row) * H + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += y[i];
+      }
+      const float4* rr = reinterpret_cast<const float4*>(du_router + static_cast<size_t>(t) * H + v * V);
+      const float4 r0 = __ldg(rr), r1 = __ldg(rr + 1);
+      acc[0] += r0.x; acc[1] += r0.y; acc[2] += r0.z; acc[3] += r0.w;
+      acc[4] += r1.x; acc[5] += r1.y; acc[6] += r1.z; acc[7] += r1.w;
+      V16::store(du + static_cast<size_t>(t) * H + v * V, acc);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- plan
+
+// One block.  Per-expert segments of the weight-gradient operands:
+// seg_start[e] = Σ_{e' < e} roundup(L_e', kSegAlign) (L = rows of the expert),
+// seg_start[E] = the total.  And the two weight-gradient GEMMs' groups, their
+// k-chunk ranges and their tile prefixes (nt2 / nt13 token tiles per group):
+//   dW2 (out[n = h, m = i] over A = act rows, B = dh rows):
+//     shared j:    A chunks from j·Tpad, B chunks from 0,         Tpad / 64
+//     routed e:    A chunks from Ks·Tpad + seg, B from Tpad + seg, padded L_e / 64
+//   dW1 / dW3 (out[n = i, m = h] over A = x rows, B = dh1 rows, one group per
+//   expert and part; part 1 (up) reads dh1 rows I..2I):
+//     shared (j, part): A from 0, B from j·Tpad
+//     routed (e, part): A from Tpad + seg, B from Ks·Tpad + seg
+// Shared groups come first (their contraction is the longest).
+__global__ void __launch_bounds__(1024) wgrad_plan_kernel(
+    const int32_t* __restrict__ offsets, int E, int Ks, int Tpad, int H, int I, int parts,
+    int32_t* __restrict__ seg_start, GroupDesc* __restrict__ g2, int4* __restrict__ k2,
+    GroupDesc* __restrict__ g13, int4* __restrict__ k13, int nt2, int nt13,
+    int* __restrict__ p2, int* __restrict__ p13) {
+  __shared__ int s_seg[1025];
+  __shared__ int warp_tot[32];
+  const int e = threadIdx.x;
+  const int len = e < E ? (offsets[e + 1] - offsets[e] + kSegAlign - 1) / kSegAlign * kSegAlign : 0;
+  // block-wide exclusive scan of len
+  const int lane = e & 31, w = e >> 5;
+  int incl = len;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int s = (lane < (blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    warp_tot[lane] = s;
+  }
+  __syncthreads();
+  const int excl = incl - len + (w > 0 ? warp_tot[w - 1] : 0);
+  if (e <= E) s_seg[e] = excl;   // thread E holds len 0: its exclusive sum is the total
+  __syncthreads();
+  if (e <= E) seg_start[e] = s_seg[e];
+  // static tile prefixes: every group of a weight-gradient GEMM has the same
+  // token-side width
+  for (int g = threadIdx.x; g <= E + Ks; g += blockDim.x) p2[g] = g * nt2;
+  for (int g = threadIdx.x; g <= (E + Ks) * parts; g += blockDim.x) p13[g] = g * nt13;
+  constexpr int kc = 64;         // elements per k-chunk
+  if (e < Ks) {
+    g2[e] = GroupDesc{0, 0, 0, 0, 1, e * H, H, 0};
+    k2[e] = make_int4(e * Tpad / kc, 0, Tpad / kc, 0);
+    for (int p = 0; p < parts; ++p) {
+      g13[e * parts + p] = GroupDesc{0, 0, 0, p * I, 2 + p, e * I, I, 0};
+      k13[e * parts + p] = make_int4(0, e * Tpad / kc, Tpad / kc, 0);
+    }
+  }
+  if (e < E) {
+    const int seg = s_seg[e], n = (s_seg[e + 1] - seg) / kc;
+    g2[Ks + e] = GroupDesc{0, 0, 0, 0, 0, e * H, H, 0};
+    k2[Ks + e] = make_int4((Ks * Tpad + seg) / kc, (Tpad + seg) / kc, n, 0);
+    for (int p = 0; p < parts; ++p) {
+      g13[(Ks + e) * parts + p] = GroupDesc{0, 0, 0, p * I, p, e * I, I, 0};
+      k13[(Ks + e) * parts + p] = make_int4((Tpad + seg) / kc, (Ks * Tpad + seg) / kc, n, 0);
+    }
+  }
+}
+
+}  // namespace moe

@@ -84,7 +84,13 @@ struct Params {
   int dense_count;               // token rows of the dense group
   int n_wtiles;                  // weight tiles (of 128 * PAIR rows) per group
   int num_k_blocks;              // ceil(K / kBK)
-  void* out[2];
+  // Optional per-group contraction range (null: every group runs k-chunks
+  // [0, num_k_blocks) of both operands).  {x, y, z} = first k-chunk of the
+  // weight operand, first k-chunk of the token operand, k-chunks (a multiple
+  // of kKPS; 0 makes the tile's output zeros).  Used by the weight-gradient
+  // GEMMs, whose contraction runs over each expert's own token rows.
+  const int4* krange;
+  void* out[4];
   int out_ld;                    // output row pitch in elements
   int out_cols;                  // valid output columns
   const float* col_offset;       // EPI_F32: per-column addend, may be null
@@ -447,7 +453,19 @@ struct Tile {
   int out_col;           // this CTA's first output column
   int n_valid;           // valid token rows of the tile
   int nt;                // token tiles of the tile's group
+  int ka0, kb0, nk;      // first k-chunk of each operand, k-chunks
 };
+
+// Group of tile t (0 for a dense group).
+__device__ __forceinline__ int group_of(const Params& p, const int* prefix, int t) {
+  if (p.groups == nullptr) return 0;
+  int lo = 0, hi = p.n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] * p.n_wtiles <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
 
 // prefix: the tile prefix staged in shared memory (unused for a dense group).
 template <int EPI, int BN, int PAIR>
@@ -455,13 +473,13 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   constexpr int kStep = Config<BN, PAIR>::kStep;
   const int nw = p.n_wtiles;
   GroupDesc d;
-  int nt, local;
+  int nt, local, lo = 0;
   if (p.groups == nullptr) {
     d = GroupDesc{0, 0, 0, 0, 0, 0, p.dense_count, 0};
     nt = (p.dense_count + BN - 1) / BN;
     local = t;
   } else {
-    int lo = 0, hi = p.n_groups;  // largest g with prefix[g] * nw <= t
+    int hi = p.n_groups;  // largest g with prefix[g] * nw <= t
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (prefix[mid] * nw <= t) lo = mid; else hi = mid;
@@ -486,6 +504,15 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.out_sel = d.out_sel;
   tl.out_row = d.out_row0 + n * th;
   tl.out_col = (w * PAIR + rank) * kCols;
+  if (p.krange != nullptr) {
+    const int4 kr = __ldg(p.krange + lo);
+    tl.ka0 = kr.x;
+    tl.kb0 = kr.y;
+    tl.nk = kr.z;
+  } else {
+    tl.ka0 = tl.kb0 = 0;
+    tl.nk = p.num_k_blocks;
+  }
   return tl;
 }
 
@@ -547,7 +574,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const int tiles_per_w = (p.groups == nullptr) ? (p.dense_count + BN - 1) / BN
                                                 : s_prefix[p.n_groups];
   const int total = p.n_wtiles * tiles_per_w;
-  const int nk = p.num_k_blocks;
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -567,7 +593,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             static_cast<uint32_t>(PAIR * kKPS) * (kABytes + static_cast<uint32_t>(b_land) * (kBK * 2));
         const uint32_t idesc = idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma));
         const CUtensorMap* bmap = &p.b[tl.b_src][tl.b_box];
-        for (int kb = 0; kb < nk; kb += kKPS) {
+        for (int kb = 0; kb < tl.nk; kb += kKPS) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
             raise_device_error(DEV_ERR_TIMEOUT_PRODUCER);
             ok = false;
@@ -586,11 +612,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           // weights: both k-blocks in one copy (chunk kb and kb + 1)
           const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
           if (EPI == EPI_SWIGLU)
-            tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), kb, pol_a);
+            tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), tl.ka0 + kb,
+                              pol_a);
           else
-            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, kb, pol_a);
+            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, tl.ka0 + kb, pol_a);
           // tokens: both k-blocks in one copy
-          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, kb, pol_keep);
+          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, tl.kb0 + kb, pol_keep);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -616,6 +643,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const int nk = p.krange != nullptr ? __ldg(p.krange + group_of(p, s_prefix, t)).z
+                                           : p.num_k_blocks;
         for (int kb = 0; kb < nk; kb += kKPS) {
           if (!mbar_wait(full_bar(stage), phase)) {
             raise_device_error(DEV_ERR_TIMEOUT_MMA);
@@ -723,6 +752,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
+          if (tl.nk == 0) {  // empty contraction: nothing was accumulated
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
           const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
           const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
           const int col = tl.out_col + q * 32 + lane;

@@ -54,6 +54,11 @@ class moe_route_outputs(ctypes.Structure):
                 ("logits", "topk_idx", "topk_w", "expert_offsets")]
 
 
+class moe_weight_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("d_centroids", "dw1", "dw3", "dw2", "dsw1", "dsw3", "dsw2")]
+
+
 _P = ctypes.c_void_p
 _S = ctypes.POINTER(moe_shape)
 _W = ctypes.POINTER(moe_weights)
@@ -75,6 +80,9 @@ _SIGNATURES = {
     "moe_dispatch_static": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P]),
     "moe_update_select_bias": (ctypes.c_int, [_S, _P, _P, ctypes.c_float, _P, _P]),
     "moe_balance_stats_workspace_size": (ctypes.c_size_t, [_S]),
+    "moe_layer_backward_workspace_size": (ctypes.c_size_t, [_S]),
+    "moe_layer_backward": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.POINTER(moe_weight_grads),
+                                          _P, ctypes.c_size_t, _P]),
     "moe_balance_stats": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -237,6 +245,24 @@ def moe_layer_forward_host(shape, weights: moe_weights, u_host, h_host, u_dev, h
         ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u_host), _ptr(h_host),
         _ptr(u_dev), _ptr(h_dev), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_backward_workspace_size(shape) -> int:
+    return lib().moe_layer_backward_workspace_size(ctypes.byref(shape_struct(shape)))
+
+
+def weight_grads(d_centroids, dw1, dw3, dw2, dsw1=None, dsw3=None, dsw2=None) -> moe_weight_grads:
+    """The gradient outputs of moe_layer_backward (fp32 tensors, or None)."""
+    return moe_weight_grads(*[_ptr(t) for t in (d_centroids, dw1, dw3, dw2, dsw1, dsw3, dsw2)])
+
+
+def moe_layer_backward(shape, weights: moe_weights, u, dh, du, grads: moe_weight_grads, ws,
+                       stream=None):
+    """du and the weight gradients of the layer for the upstream gradient dh."""
+    _check("moe_layer_backward", lib().moe_layer_backward(
+        ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u), _ptr(dh), _ptr(du),
+        ctypes.byref(grads), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:

@@ -1,5 +1,5 @@
 /*
- * moe.h — C ABI of the B300 (sm_103a) DeepSeekMoE layer forward.
+ * moe.h — C ABI of the B300 (sm_103a) DeepSeekMoE layer forward and backward.
  *
  * The layer computed here (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE",
  * llm-infra-atlas, §3.1 Eq. 9–11; DeepSeek-V3 form Eq. 12–15):
@@ -249,6 +249,42 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* shape,
                                           void* u_dev, void* h_dev, void* ws,
                                           size_t ws_bytes,
                                           moe_stream_t stream);
+
+/* Weight gradients of moe_layer_backward (device pointers, fp32, written, not
+ * accumulated): d_centroids [E, H]; dw1, dw3 [E, I, H]; dw2 [E, H, I]; the
+ * shared experts' dsw1, dsw3 [Ks, I, H] and dsw2 [Ks, H, I] (NULL when
+ * n_shared = 0); dw3 and dsw3 are NULL for ReLU. */
+typedef struct {
+  float* d_centroids;
+  float *dw1, *dw3, *dw2;
+  float *dsw1, *dsw3, *dsw2;
+} moe_weight_grads;
+
+/* Backward of moe_layer_forward for the upstream gradient dh = dL/dh [T, H]
+ * (bf16): du = dL/du [T, H] (bf16 out) and the weight gradients `grads`.
+ * The forward is h_t = u_t + Σ_j FFN_j^shared(u_t) + Σ_s g_{t,s}
+ * FFN_{idx[t,s]}(u_t) (page "02 · 细粒度 MoE", §3.1 Eq. 9–15; expert FFN as on
+ * page "19-deepseek-moe"), differentiated with the chosen experts held fixed:
+ * the top-k choice is piecewise constant in the logits, so gradients reach
+ * the router only through the gate weights g, and select_bias (which only
+ * changes the choice) gets none.  logit_offset is read like the forward
+ * reads it (no gradient is returned for it).
+ *   du_t = dh_t + Σ_j J_j^T dh_t + Σ_s g_{t,s} J_{idx}^T dh_t + Σ_i dz_{t,i} e_i,
+ *   dg_{t,s} = <dh_t, FFN_{idx[t,s]}(u_t)>, dz = dL/dlogits through softmax
+ *   (no renormalisation) or the normalised sigmoid, d e_i = Σ_t dz_{t,i} u_t.
+ * The call recomputes the forward's routing and the experts' pre-activations
+ * from u (nothing is saved between the two calls), so it needs only the
+ * forward's inputs.  fp32 accumulation; the intermediates (pre-activations,
+ * per-row gradients, transposed operands) are bf16, as in the forward.
+ * bf16 layers only, with inter % 128 == 0 and (n_routed + n_shared) x (2 for
+ * SwiGLU, else 1) <= 1024 (otherwise MOE_ERR_UNSUPPORTED).  T = 0 writes
+ * zero gradients.  ws: moe_layer_backward_workspace_size bytes. */
+MOE_API size_t moe_layer_backward_workspace_size(const moe_shape* shape);
+MOE_API moe_status moe_layer_backward(const moe_shape* shape,
+                                      const moe_weights* weights, const void* u,
+                                      const void* dh, void* du,
+                                      const moe_weight_grads* grads, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream);
 
 /* moe_dispatch without a workspace argument, for callers that cannot
  * allocate device memory: a runtime whose allocator already owns all of the

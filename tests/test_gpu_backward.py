@@ -1,0 +1,148 @@
+"""Layer backward on the GPU against the oracle's backward.
+
+The kernels recompute the forward's routing; the test reads the same
+routing from a forward call (same kernels, same inputs) and gives the oracle
+that choice, so both sides differentiate the same piecewise-smooth function.
+Every gradient tensor is compared element by element at sizes that span
+several tiles, ragged tails, experts that nobody chose, the shared-only and
+single-token cases; the bar is the layer's bf16 one, max|Δ| ≤ 2e-2 · max|ref|
+per tensor (the backward's intermediates are bf16 like the forward's)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.moe_oracle as O
+from fine_grained_shared_gemm_b300 import moe as M
+from fine_grained_shared_gemm_b300 import workloads as W
+from parity_helpers import TOL, assert_close, expert_fns, np64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _shape(name, **kw):
+    base = dict(T=200, H=256, n_routed=8, n_shared=1, top_k=2, inter=256, gate=W.GATE_SOFTMAX,
+                act=W.ACT_SWIGLU, dtype="bf16")
+    base.update(kw)
+    return W.MoEShape(name, **base)
+
+
+SHAPES = [
+    _shape("bwd_softmax_swiglu"),
+    _shape("bwd_sigmoid_relu_noshared", T=333, n_routed=16, n_shared=0, top_k=4, inter=128,
+           gate=W.GATE_SIGMOID_BIAS, act=W.ACT_RELU, bias_range=0.1),
+    _shape("bwd_multitile", T=600, H=512, n_routed=6, n_shared=1, top_k=2, inter=384),
+    _shape("bwd_narrow_tiles", T=64, H=384, n_routed=32, n_shared=2, top_k=2, inter=128,
+           gate=W.GATE_SIGMOID_BIAS, bias_range=0.1),
+    _shape("bwd_skewed_empty_experts", T=300, n_routed=12, n_shared=1, top_k=3, inter=128,
+           gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, logit_offset_std=3.0),
+    _shape("bwd_shared_only", T=130, n_routed=4, n_shared=2, top_k=0, inter=128),
+    _shape("bwd_one_token", T=1, n_routed=8, n_shared=1, top_k=2, inter=128),
+]
+
+
+def grads_buffers(shape):
+    E, Ks, H, I = shape.n_routed, shape.n_shared, shape.H, shape.inter
+    sw = shape.act == W.ACT_SWIGLU
+    f = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device=DEV)
+    g = dict(d_centroids=f(E, H), dw1=f(E, I, H), dw3=f(E, I, H) if sw else None, dw2=f(E, H, I),
+             dsw1=f(Ks, I, H) if Ks else None, dsw3=f(Ks, I, H) if Ks and sw else None,
+             dsw2=f(Ks, H, I) if Ks else None)
+    return g
+
+
+def run_backward(shape, inp, dh):
+    g = grads_buffers(shape)
+    du = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = M.alloc_workspace(M.moe_layer_backward_workspace_size(shape), DEV)
+    M.moe_layer_backward(shape, M.weights_struct(inp), inp.u, dh, du,
+                         M.weight_grads(g["d_centroids"], g["dw1"], g["dw3"], g["dw2"],
+                                        g["dsw1"], g["dsw3"], g["dsw2"]), ws)
+    st, code = M.moe_device_status()
+    assert st == M.MOE_OK, (st, code)
+    return du, g
+
+
+def forward_routing(shape, inp):
+    T, E, k = shape.T, shape.n_routed, shape.top_k
+    ws = M.alloc_workspace(M.moe_layer_workspace_size(shape), DEV)
+    h = torch.empty((T, shape.H), dtype=torch.bfloat16, device=DEV)
+    ro = dict(logits=torch.empty((T, E), dtype=torch.float32, device=DEV),
+              topk_idx=torch.empty((T, k), dtype=torch.int32, device=DEV))
+    M.moe_layer_forward(shape, M.weights_struct(inp), inp.u, h, ws, route_out=ro)
+    return ro["logits"].cpu().numpy(), ro["topk_idx"].cpu().numpy().astype(np.int64)
+
+
+def oracle_backward(shape, inp, dh, z, idx):
+    routed, shared = expert_fns(inp)
+    return O.layer_backward(np64(inp.u), np64(dh), np64(inp.centroids), z, idx, shape.gate,
+                            routed, shared, shape.n_routed, shape.n_shared, shape.act)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_layer_backward_matches_oracle(shape):
+    inp = W.make_inputs(shape, DEV, seed=0)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    du, g = run_backward(shape, inp, dh)
+    torch.cuda.synchronize()
+    z, idx = forward_routing(shape, inp)
+    ref = oracle_backward(shape, inp, dh, z, idx)
+    tol = TOL["bf16"]
+    assert_close(np64(du), ref["du"], tol, "du")
+    if shape.top_k > 0:
+        assert_close(np64(g["d_centroids"]), ref["d_centroids"], tol, "d_centroids")
+    else:
+        assert not g["d_centroids"].any()
+    for key in ("dw1", "dw3", "dw2", "dsw1", "dsw3", "dsw2"):
+        if g[key] is None:
+            assert ref[key] is None or ref[key].size == 0, key
+            continue
+        got = np64(g[key])
+        assert np.isfinite(got).all(), key
+        if ref[key] is None or not np.abs(ref[key]).any():
+            assert not got.any(), key        # nobody chose any expert: exact zeros
+        else:
+            assert_close(got, ref[key], tol, key)
+    # experts nobody chose get exact zeros
+    counts = np.bincount(idx.reshape(-1), minlength=shape.n_routed) if shape.top_k else \
+        np.zeros(shape.n_routed, np.int64)
+    for e in np.nonzero(counts == 0)[0]:
+        for key in ("dw1", "dw3", "dw2"):
+            if g[key] is not None:
+                assert not g[key][e].any(), (key, e)
+
+
+def test_skewed_case_has_empty_experts():
+    """The skewed shape above really exercises empty experts (zero-length
+    contractions in the weight-gradient GEMMs)."""
+    shape = [s for s in SHAPES if s.name == "bwd_skewed_empty_experts"][0]
+    inp = W.make_inputs(shape, DEV, seed=0)
+    _, idx = forward_routing(shape, inp)
+    counts = np.bincount(idx.reshape(-1), minlength=shape.n_routed)
+    assert (counts == 0).any(), counts
+
+
+def test_layer_backward_is_deterministic():
+    shape = SHAPES[2]
+    inp = W.make_inputs(shape, DEV, seed=0)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(2)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    du1, g1 = run_backward(shape, inp, dh)
+    du2, g2 = run_backward(shape, inp, dh)
+    torch.cuda.synchronize()
+    assert torch.equal(du1, du2)
+    for key in g1:
+        if g1[key] is not None:
+            assert torch.equal(g1[key], g2[key]), key
+
+
+def test_backward_rejects_unsupported_shapes():
+    bad = _shape("bwd_f32", dtype="f32", inter=128)
+    assert M.moe_layer_backward_workspace_size(bad) == 0
+    odd = _shape("bwd_odd_inter", inter=192)
+    assert M.moe_layer_backward_workspace_size(odd) == 0
