@@ -234,6 +234,67 @@ class Layer:
         M.moe_combine(s, i.u, self.y_perm, self.y_shared, self.w, self.slot_row, self.h)
 
 
+def backward_launches(s: W.MoEShape) -> int:
+    """Kernel launches of one moe_layer_backward call (counted from its host code)."""
+    sw = s.act == W.ACT_SWIGLU
+    n = 2 + (4 if s.top_k else 2)                 # logits, route, dispatch
+    n += 2 if s.top_k else 0                      # gather dh rows, row gate weights
+    n += 1                                        # FFN plan
+    n += (3 if sw else 2) * (1 + (s.n_shared > 0))  # weight transposes
+    n += 3 if sw else 2                           # pre-activations and dh W2
+    n += 1 + 1 + 2 + 1 + 1                        # act bwd, gate bwd, router grads, dx, du
+    n += 1 + 2 + 2 * s.n_shared + (4 if s.top_k else 0)  # plan, operand transposes
+    n += 2                                        # weight-gradient GEMMs
+    return n
+
+
+def measure_backward(args, shape, layer, flush, dev, peaks):
+    """moe_layer_backward at the same workload: device time per call (L2
+    flushed between calls), algorithmic FLOPs = 2 x the forward's expert
+    FLOPs (input and weight gradients) + 4·T·E·H for the router."""
+    need = M.moe_layer_backward_workspace_size(shape)
+    if need == 0:
+        return None
+    s, inp = shape, layer.inp
+    E, Ks, H, I = s.n_routed, s.n_shared, s.H, s.inter
+    sw = s.act == W.ACT_SWIGLU
+    f = lambda *d: torch.empty(d, dtype=torch.float32, device=dev)
+    g = [f(E, H), f(E, I, H), f(E, I, H) if sw else None, f(E, H, I),
+         f(Ks, I, H) if Ks else None, f(Ks, I, H) if Ks and sw else None,
+         f(Ks, H, I) if Ks else None]
+    grads = M.weight_grads(*g)
+    ws = M.alloc_workspace(need, dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    dh = torch.randn((s.T, H), generator=gen, device=dev).to(s.torch_dtype)
+    du = torch.empty_like(dh)
+    for _ in range(args.warmup):
+        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code} in the backward")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    flops = 2 * expert_flops(s) + 4 * s.T * E * H
+    tf = flops / (ms / 1e3) / 1e12
+    del ws, g, grads
+    return {"tokens_per_s": round(s.T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+            "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "gpu_launches": backward_launches(s) * K,
+            "note": "recomputes routing and the gate/up pre-activations from u; "
+                    "weight gradients fp32"}
+
+
 def run_cuda(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -330,6 +391,8 @@ def run_cuda(args):
         "gpu_launches": layer.launches_per_step * K,
         "clocks": clk.summary(),
     }
+    if not args.no_backward:
+        line["backward"] = measure_backward(args, shape, layer, flush, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, layer, args.cpu_sample)
     if rank == 0:
@@ -452,6 +515,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the timed moe_layer_backward leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -46,11 +46,16 @@ constexpr int kSegAlign = 128;
 // blockIdx.z selects a matrix of a batch (src/dst advance by their strides).
 // cols (the features, dst rows) % 64 == 0; dst_ld, col0 and the strides are
 // multiples of 8 elements.
+// dst_rows == 0: dst is row-major with row pitch dst_ld.  dst_rows > 0: dst
+// is chunk-major, the layout the weight-gradient GEMMs read: element (c, j)
+// at ((j / 64) · dst_rows + c) · 64 + j % 64, so that one 64-column chunk of
+// all dst_rows rows is contiguous and a TMA box of rows reads one block
+// (col0 % 64 == 0).
 __global__ void __launch_bounds__(256) transpose_kernel(
     const __nv_bfloat16* __restrict__ src, int src_ld, long long src_bstride, int cols,
     int rows_total, const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets,
     int E, __nv_bfloat16* __restrict__ dst, long long dst_ld, long long col0,
-    long long dst_bstride) {
+    long long dst_bstride, long long dst_rows) {
   __shared__ uint16_t tile[64][66];
   const int j0 = blockIdx.x * 64;   // first dst column (relative to col0)
   const int c0 = blockIdx.y * 64;   // first feature
@@ -90,7 +95,10 @@ __global__ void __launch_bounds__(256) transpose_kernel(
     uint16_t* h = reinterpret_cast<uint16_t*>(&x);
 #pragma unroll
     for (int q = 0; q < 8; ++q) h[q] = tile[v * 8 + q][c];
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c0 + c) * dst_ld + col0 + j0 + v * 8) = x;
+    const size_t at = dst_rows > 0
+        ? (static_cast<size_t>((col0 + j0) >> 6) * dst_rows + c0 + c) * 64 + v * 8
+        : static_cast<size_t>(c0 + c) * dst_ld + col0 + j0 + v * 8;
+    *reinterpret_cast<uint4*>(dst + at) = x;
   }
 }
 
@@ -253,25 +261,31 @@ __global__ void __launch_bounds__(256) gate_backward_kernel(
 // element (m, k) at a[m * sam + k * sak], B bf16 [K, N] row-major, out fp32
 // [M, N] row-major.  64 x 64 output tiles, 4 x 4 per thread, K in steps of 16.
 // Used for dz · centroids (A = dz, sam = E, sak = 1) and dzᵀ · u (sam = 1,
-// sak = E).
+// sak = E).  blockIdx.z splits K into gridDim.z ranges of k_chunk; split z
+// writes its partial sums to out + z · M · N (reduced by
+// split_reduce_kernel in split order).
 __global__ void __launch_bounds__(256) router_grad_kernel(const float* __restrict__ a,
                                                           long long sam, long long sak,
                                                           const __nv_bfloat16* __restrict__ b,
-                                                          int M, int N, int K,
+                                                          int M, int N, int K, int k_chunk,
                                                           float* __restrict__ out) {
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int k_begin = blockIdx.z * k_chunk, k_end = min(K, k_begin + k_chunk);
+  out += static_cast<size_t>(blockIdx.z) * M * N;
+  const bool k_inner = sak == 1;   // A rows contiguous along k: load along k
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += 16) {
+  for (int k0 = k_begin; k0 < k_end; k0 += 16) {
     for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-      const int kk = i >> 6, mm = i & 63;   // A: consecutive threads along m
+      const int kk = k_inner ? (i & 15) : (i >> 6);
+      const int mm = k_inner ? (i >> 4) : (i & 63);
       const int m = m0 + mm, kx = k0 + kk;
-      As[kk][mm] = (m < M && kx < K) ? __ldg(a + m * sam + kx * sak) : 0.0f;
-      const int nn = i & 63;
-      const int n = n0 + nn;
-      Bs[kk][nn] = (n < N && kx < K) ? __bfloat162float(b[static_cast<size_t>(kx) * N + n]) : 0.0f;
+      As[kk][mm] = (m < M && kx < k_end) ? __ldg(a + m * sam + kx * sak) : 0.0f;
+      const int kb = i >> 6, nn = i & 63;
+      const int n = n0 + nn, kbx = k0 + kb;
+      Bs[kb][nn] = (n < N && kbx < k_end) ? __bfloat162float(b[static_cast<size_t>(kbx) * N + n]) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -297,6 +311,18 @@ __global__ void __launch_bounds__(256) router_grad_kernel(const float* __restric
       const int n = n0 + tx * 4 + j;
       if (n < N) out[static_cast<size_t>(m) * N + n] = acc[i][j];
     }
+  }
+}
+
+// out[i] = Σ_{z < splits} part[z · n + i], z ascending.
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part,
+                                                           int splits, long long n,
+                                                           float* __restrict__ out) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float acc = 0.0f;
+    for (int z = 0; z < splits; ++z) acc += part[z * n + i];
+    out[i] = acc;
   }
 }
 

@@ -136,6 +136,17 @@ moe_status make_map3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   return encode(m, 3, base, dims, strides, box);
 }
 
+// Chunk-major bf16 operand (element (r, k) at ((k / 64) · rows + r) · 64 + k % 64,
+// n_chunks chunks of 64 columns): the same (64 columns, rows, chunks) view
+// as make_map3, with each chunk a contiguous block of rows x 128 bytes.
+moe_status make_map3_chunked(CUtensorMap* m, const void* base, uint64_t rows, uint64_t n_chunks,
+                             uint32_t box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::kBK), rows, n_chunks};
+  const cuuint64_t strides[2] = {tc::kBK * 2, rows * tc::kBK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(tc::kBK), box_rows, tc::kKPS};
+  return encode(m, 3, base, dims, strides, box);
+}
+
 // SwiGLU gate and up stacks w1, w3 (both bf16 [rows, cols], rows % 64 == 0)
 // as one 5-D tensor (64 columns, 64 rows, {first, second} stack, 64-row
 // blocks, cols / 64 chunks) whose third dimension steps between the two
@@ -167,6 +178,13 @@ moe_status make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_
 // Token-source maps for every box height.
 moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, uint64_t cols) {
   for (int i = 0; i < tc::kNumBoxes; ++i) MOE_TRY(make_map3(&maps[i], base, rows, cols, 16u << i));
+  return MOE_OK;
+}
+
+moe_status make_token_maps_chunked(CUtensorMap* maps, const void* base, uint64_t rows,
+                                   uint64_t n_chunks) {
+  for (int i = 0; i < tc::kNumBoxes; ++i)
+    MOE_TRY(make_map3_chunked(&maps[i], base, rows, n_chunks, 16u << i));
   return MOE_OK;
 }
 
@@ -813,6 +831,7 @@ struct BwdWs {
   float *row_gate, *dg_row;              // [Tk]
   float* dz;                             // [T, E]
   float* du_router;                      // [T, H]
+  float* cent_part;                      // [splits, E, H]
   __nv_bfloat16 *dx_perm, *dx_sh;        // [Tk, H], [Ks·T, H]
   __nv_bfloat16 *w2t, *sw2t;             // [E, I, H], [Ks, I, H]
   __nv_bfloat16 *w13t, *sw13t;           // [E, H, P·I], [Ks, H, P·I]
@@ -825,6 +844,19 @@ struct BwdWs {
   long long Tpad, KX, KA;
   size_t total;
 };
+
+// Splits of T for the centroid gradient: enough 64 x 64 tiles x splits for
+// about four waves, each split at least 256 tokens, at most kMaxCentSplits;
+// the result depends only on the shape (fixed summation order).
+constexpr int kMaxCentSplits = 32;
+
+int cent_splits(const moe_shape* s) {
+  const int tiles = cdiv(s->H, 64) * cdiv(s->n_routed, 64);
+  const int want = std::max(1, std::min(cdiv(4 * 148, tiles), cdiv(std::max(s->T, 1), 256)));
+  const int splits = std::min(want, kMaxCentSplits);
+  const int k_chunk = cdiv(cdiv(std::max(s->T, 1), splits), 16) * 16;
+  return cdiv(std::max(s->T, 1), k_chunk);
+}
 
 BwdWs carve_bwd(void* ws, const moe_shape* s) {
   const size_t T = s->T, E = s->n_routed, k = s->top_k, Ks = s->n_shared, H = s->H,
@@ -870,6 +902,7 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.dg_row = static_cast<float*>(take(Tk * 4));
   B.dz = static_cast<float*>(take(T * E * 4));
   B.du_router = static_cast<float*>(take(T * H * 4));
+  B.cent_part = static_cast<float*>(take(static_cast<size_t>(cent_splits(s)) * E * H * 4));
   B.dx_perm = bf(Tk * H);
   B.dx_sh = bf(Ks * T * H);
   B.w2t = bf(E * I * H);
@@ -916,22 +949,23 @@ moe_status transpose_weights(const void* src, int R, int C, int batch, __nv_bflo
   dim3 grid(R / 64, C / 64, batch);
   transpose_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
                                          static_cast<long long>(R) * C, C, R, nullptr, nullptr, 0,
-                                         dst, dst_ld, col0, dst_bstride);
+                                         dst, dst_ld, col0, dst_bstride, 0);
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
 
-// Token rows into the K-major weight-gradient operands: rows [0, n) of src
-// (row pitch = cols) into dst columns [col0, col0 + roundup(n, 64)), zeros
-// past n; with seg_start, the routed rows into per-expert segments.
+// Token rows into the chunk-major K-major weight-gradient operands (cols
+// rows of features): rows [0, n) of src (row pitch = cols) into dst columns
+// [col0, col0 + roundup(n, 64)), zeros past n; with seg_start, the routed
+// rows into per-expert segments.
 moe_status transpose_rows(const __nv_bfloat16* src, int cols, int n, const int32_t* seg_start,
                           const int32_t* offsets, int E, int max_cols, __nv_bfloat16* dst,
-                          long long dst_ld, long long col0, cudaStream_t st) {
+                          long long col0, cudaStream_t st) {
   if (max_cols <= 0) return MOE_OK;
-  if (cols % 64 || dst_ld % 8 || col0 % 8 || !al16(src) || !al16(dst)) return MOE_ERR_INVALID_ARG;
+  if (cols % 64 || col0 % 64 || !al16(src) || !al16(dst)) return MOE_ERR_INVALID_ARG;
   dim3 grid(cdiv(max_cols, 64), cols / 64, 1);
   transpose_kernel<<<grid, 256, 0, st>>>(src, cols, 0, cols, n, seg_start, offsets, E, dst,
-                                         dst_ld, col0, 0);
+                                         0, col0, 0, cols);
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -1068,12 +1102,24 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     else MOE_GATE_BWD(32);
 #undef MOE_GATE_BWD
     MOE_CUDA(cudaGetLastError());
-    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(T, 64)), 256, 0, st>>>(
-        B.dz, E, 1, static_cast<const __nv_bfloat16*>(wt->centroids), T, H, E, B.du_router);
+    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(T, 64), 1), 256, 0, st>>>(
+        B.dz, E, 1, static_cast<const __nv_bfloat16*>(wt->centroids), T, H, E, E, B.du_router);
     MOE_CUDA(cudaGetLastError());
-    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(E, 64)), 256, 0, st>>>(
-        B.dz, 1, E, static_cast<const __nv_bfloat16*>(u), E, H, T, gr->d_centroids);
+    // dzᵀ u contracts over all T tokens: split T so the grid fills the GPU,
+    // then add the partial sums in split order
+    const int splits = cent_splits(s);
+    const int k_chunk = cdiv(cdiv(T, splits), 16) * 16;
+    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(E, 64), splits), 256, 0, st>>>(
+        B.dz, 1, E, static_cast<const __nv_bfloat16*>(u), E, H, T, k_chunk,
+        splits > 1 ? B.cent_part : gr->d_centroids);
     MOE_CUDA(cudaGetLastError());
+    if (splits > 1) {
+      const long long n = static_cast<long long>(E) * H;
+      split_reduce_kernel<<<static_cast<int>(std::min<long long>(cdiv(static_cast<int>(n), 256),
+                                                                  num_sms() * 8)),
+                            256, 0, st>>>(B.cent_part, splits, n, gr->d_centroids);
+      MOE_CUDA(cudaGetLastError());
+    }
   }
 
   // ---- dx = dh1 [W1; W3] per expert row, then du
@@ -1114,29 +1160,29 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   const int rmax = static_cast<int>(B.KX - B.Tpad);
   const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
   MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(u), H, T, nullptr, nullptr, 0,
-                         static_cast<int>(tpad), B.xT, B.KX, 0, st));
+                         static_cast<int>(tpad), B.xT, 0, st));
   MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(dh), H, T, nullptr, nullptr, 0,
-                         static_cast<int>(tpad), B.dT, B.KX, 0, st));
+                         static_cast<int>(tpad), B.dT, 0, st));
   for (int j = 0; j < Ks; ++j) {
     const size_t r0 = static_cast<size_t>(Tk) + static_cast<size_t>(j) * T;
     MOE_TRY(transpose_rows(B.actg + r0 * I, I, T, nullptr, nullptr, 0, static_cast<int>(tpad),
-                           B.aT, B.KA, j * tpad, st));
+                           B.aT, j * tpad, st));
     MOE_TRY(transpose_rows(B.dh1 + r0 * PI, static_cast<int>(PI), T, nullptr, nullptr, 0,
-                           static_cast<int>(tpad), B.d1T, B.KA, j * tpad, st));
+                           static_cast<int>(tpad), B.d1T, j * tpad, st));
   }
   if (Tk > 0) {
-    MOE_TRY(transpose_rows(B.x_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.xT, B.KX, tpad, st));
-    MOE_TRY(transpose_rows(B.d_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.dT, B.KX, tpad, st));
-    MOE_TRY(transpose_rows(B.actg, I, Tk, B.seg_start, B.offsets, E, rmax, B.aT, B.KA, sh, st));
+    MOE_TRY(transpose_rows(B.x_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.xT, tpad, st));
+    MOE_TRY(transpose_rows(B.d_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.dT, tpad, st));
+    MOE_TRY(transpose_rows(B.actg, I, Tk, B.seg_start, B.offsets, E, rmax, B.aT, sh, st));
     MOE_TRY(transpose_rows(B.dh1, static_cast<int>(PI), Tk, B.seg_start, B.offsets, E, rmax,
-                           B.d1T, B.KA, sh, st));
+                           B.d1T, sh, st));
   }
   {  // dW2[e][h][i] = Σ_r dh_r[h] · (g act)_r[i]
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3(&p.a[0], B.aT, I, B.KA, tc::kBM));
+    MOE_TRY(make_map3_chunked(&p.a[0], B.aT, I, B.KA / 64, tc::kBM));
     p.a[1] = p.a[0];
-    MOE_TRY(make_token_maps(p.b[0], B.dT, H, B.KX));
+    MOE_TRY(make_token_maps_chunked(p.b[0], B.dT, H, B.KX / 64));
     memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
     p.groups = B.wg2;
     p.tile_prefix = B.wp2;
@@ -1152,9 +1198,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   {  // dW1[e][i][h] = Σ_r da_r[i] · x_r[h], dW3 likewise with dc
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3(&p.a[0], B.xT, H, B.KX, tc::kBM));
+    MOE_TRY(make_map3_chunked(&p.a[0], B.xT, H, B.KX / 64, tc::kBM));
     p.a[1] = p.a[0];
-    MOE_TRY(make_token_maps(p.b[0], B.d1T, PI, B.KA));
+    MOE_TRY(make_token_maps_chunked(p.b[0], B.d1T, PI, B.KA / 64));
     memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
     p.groups = B.wg13;
     p.tile_prefix = B.wp13;

@@ -29,7 +29,9 @@
 //   warp 0      TMA producer (one thread)
 //   warp 1      TMEM allocation and (leader only) MMA issue (one thread)
 //   warps 2..5  epilogue: TMEM -> registers (activation fused in) -> bf16
-//               tile in shared memory -> TMA bulk store
+//               tile in shared memory -> TMA bulk store; fp32 outputs (router
+//               logits, weight gradients) go straight from registers, one
+//               128-byte row segment per warp store
 //
 // The producer hands the MMA thread each stage's instruction descriptor
 // through shared memory, so the MMA thread never decodes tiles; the per-group
@@ -752,26 +754,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
-          if (tl.nk == 0) {  // empty contraction: nothing was accumulated
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
-          }
-          const bool row_ok = c0 + lane < tl.n_valid && cols_ok;
-          const size_t orow = static_cast<size_t>(tl.out_row + c0 + lane);
+          // lane = output column: for each token row j the warp writes 32
+          // consecutive fp32 columns (128 bytes) of that row
           const int col = tl.out_col + q * 32 + lane;
+          const bool col_ok = cols_ok && col < p.out_cols;
           const float add =
-              (p.col_offset != nullptr && col < p.out_cols) ? __ldg(p.col_offset + col) : 0.0f;
+              (p.col_offset != nullptr && col_ok) ? __ldg(p.col_offset + col) : 0.0f;
+          float* o = static_cast<float*>(p.out[tl.out_sel]) +
+                     static_cast<size_t>(tl.out_row + c0) * p.out_ld + col;
+          if (col_ok) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]) + add;
-          __syncwarp();
-          if (row_ok) {
-            float* o = static_cast<float*>(p.out[tl.out_sel]) + orow * p.out_ld;
-            const int c_begin = tl.out_col + q * 32;
-#pragma unroll 4
             for (int j = 0; j < 32; ++j)
-              if (c_begin + j < p.out_cols) o[c_begin + j] = buf[lane * 33 + j];
+              if (j < nrow)
+                o[static_cast<size_t>(j) * p.out_ld] =
+                    tl.nk == 0 ? 0.0f : __uint_as_float(v[j]) + add;
           }
-          __syncwarp();
         } else {
           emit([&](int j) {
             const float x = __uint_as_float(v[j]);
