@@ -240,7 +240,6 @@ def backward_launches(s: W.MoEShape) -> int:
     n = 2 + (4 if s.top_k else 2)                 # logits, route, dispatch
     n += 2 if s.top_k else 0                      # gather dh rows, row gate weights
     n += 1                                        # FFN plan
-    n += (3 if sw else 2) * (1 + (s.n_shared > 0))  # weight transposes
     n += 3 if sw else 2                           # pre-activations and dh W2
     n += 1 + 1 + 2 + 1 + 1                        # act bwd, gate bwd, router grads, dx, du
     n += 1 + 2 + 2 * s.n_shared + (4 if s.top_k else 0)  # plan, operand transposes

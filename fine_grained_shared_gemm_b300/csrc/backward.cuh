@@ -5,11 +5,12 @@
 // fixed: the top-k choice is piecewise constant in the logits and the
 // selection bias only changes the choice, so neither passes a gradient.
 //
-// The tensor-core grouped GEMM does the contractions (both operands K-major);
-// the kernels here produce its operands and consume its outputs:
-//   transpose_kernel       weights and token rows into K-major operands (the
-//                          weight gradients contract over each expert's own
-//                          token rows, padded per expert to kSegAlign zeros)
+// The tensor-core grouped GEMM does the contractions (the input-gradient
+// GEMMs read the weights MN-major, in their stored layout); the kernels here
+// produce its other operands and consume its outputs:
+//   transpose_kernel       token rows into K-major operands for the weight
+//                          gradients, which contract over each expert's own
+//                          token rows (padded per expert to kSegAlign zeros)
 //   act_backward_kernel    SwiGLU / ReLU derivative per row, the gate-scaled
 //                          activation for dW2 and the per-row <dy, y> for the
 //                          gate gradient
@@ -35,32 +36,26 @@ constexpr int kSegAlign = 128;
 
 // ---------------------------------------------------------------- transposes
 
-// dst[c][col0 + j] = src[row(j)][c] for 64 x 64 tiles through shared memory.
-// Two layouts of the j -> row map:
-//   seg_start == nullptr, rows_total >= 0: row(j) = j, columns j >= rows_total
-//     (up to the grid's width) are written as zeros;
+// dst[c][col0 + j] = src[row(j)][c] for 64 x 64 tiles through shared memory,
+// src row-major with row pitch `cols`, dst chunk-major — the layout the
+// weight-gradient GEMMs read: element (c, j) at ((j / 64) · cols + c) · 64 +
+// j % 64, so that one 64-column chunk of all `cols` rows is contiguous and a
+// TMA box of rows reads one block (col0 % 64 == 0).  Two layouts of the
+// j -> row map:
+//   seg_start == nullptr: row(j) = j; columns j >= rows_total (up to the
+//     grid's width) are written as zeros;
 //   seg_start != nullptr: the columns are per-expert segments: expert e owns
 //     [seg_start[e], seg_start[e+1]) and row(j) = offsets[e] + j - seg_start[e]
 //     while that is below offsets[e+1], zeros after; tiles at or past
 //     seg_start[E] write nothing.
-// blockIdx.z selects a matrix of a batch (src/dst advance by their strides).
-// cols (the features, dst rows) % 64 == 0; dst_ld, col0 and the strides are
-// multiples of 8 elements.
-// dst_rows == 0: dst is row-major with row pitch dst_ld.  dst_rows > 0: dst
-// is chunk-major, the layout the weight-gradient GEMMs read: element (c, j)
-// at ((j / 64) · dst_rows + c) · 64 + j % 64, so that one 64-column chunk of
-// all dst_rows rows is contiguous and a TMA box of rows reads one block
-// (col0 % 64 == 0).
+// cols % 64 == 0.
 __global__ void __launch_bounds__(256) transpose_kernel(
-    const __nv_bfloat16* __restrict__ src, int src_ld, long long src_bstride, int cols,
-    int rows_total, const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets,
-    int E, __nv_bfloat16* __restrict__ dst, long long dst_ld, long long col0,
-    long long dst_bstride, long long dst_rows) {
+    const __nv_bfloat16* __restrict__ src, int cols, int rows_total,
+    const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets, int E,
+    __nv_bfloat16* __restrict__ dst, long long col0) {
   __shared__ uint16_t tile[64][66];
   const int j0 = blockIdx.x * 64;   // first dst column (relative to col0)
   const int c0 = blockIdx.y * 64;   // first feature
-  src += blockIdx.z * src_bstride;
-  dst += blockIdx.z * dst_bstride;
   int row0, valid;                  // source row of column j0, valid columns of the tile
   if (seg_start == nullptr) {
     row0 = j0;
@@ -81,7 +76,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(
     const int r = i >> 3, v = i & 7;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if (r < valid)
-      x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row0 + r) * src_ld +
+      x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row0 + r) * cols +
                                                c0 + v * 8));
     const uint16_t* h = reinterpret_cast<const uint16_t*>(&x);
 #pragma unroll
@@ -95,9 +90,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(
     uint16_t* h = reinterpret_cast<uint16_t*>(&x);
 #pragma unroll
     for (int q = 0; q < 8; ++q) h[q] = tile[v * 8 + q][c];
-    const size_t at = dst_rows > 0
-        ? (static_cast<size_t>((col0 + j0) >> 6) * dst_rows + c0 + c) * 64 + v * 8
-        : static_cast<size_t>(c0 + c) * dst_ld + col0 + j0 + v * 8;
+    const size_t at = (static_cast<size_t>((col0 + j0) >> 6) * cols + c0 + c) * 64 + v * 8;
     *reinterpret_cast<uint4*>(dst + at) = x;
   }
 }

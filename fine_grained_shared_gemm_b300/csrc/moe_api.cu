@@ -147,6 +147,32 @@ moe_status make_map3_chunked(CUtensorMap* m, const void* base, uint64_t rows, ui
   return encode(m, 3, base, dims, strides, box);
 }
 
+// A weight stack bf16 [rows, cols] row-major read MN-major (the operand is its
+// transpose): (64 columns, rows, cols / 64 column blocks), box 64 columns x
+// kKPS·64 rows x 2 column blocks, landing [block][row][64] (two slabs).
+moe_status make_map3_mn(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::kBK), rows, cols / tc::kBK};
+  const cuuint64_t strides[2] = {cols * 2, tc::kBK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(tc::kBK), tc::kKPS * tc::kBK, 2};
+  return encode(m, 3, base, dims, strides, box);
+}
+
+// Two stacks w1, w3 (bf16 [rows, cols] each) read MN-major one after the
+// other along k: (64 columns, rows, 2 stacks, cols / 64 blocks), the stack
+// dimension stepping between the two allocations (< 2^40 bytes apart).
+// *swap: the lower-addressed allocation (the map's first stack) is w3.
+moe_status make_map4_mn_pair(CUtensorMap* m, const void* w1, const void* w3, uint64_t rows,
+                             uint64_t cols, int* swap) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w1), b = reinterpret_cast<uintptr_t>(w3);
+  *swap = b < a;
+  const uintptr_t gap = b < a ? a - b : b - a;
+  if (gap == 0 || gap >= (static_cast<uintptr_t>(1) << 40)) return MOE_ERR_UNSUPPORTED;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(tc::kBK), rows, 2, cols / tc::kBK};
+  const cuuint64_t strides[3] = {cols * 2, static_cast<cuuint64_t>(gap), tc::kBK * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(tc::kBK), tc::kKPS * tc::kBK, 1, 2};
+  return encode(m, 4, b < a ? w3 : w1, dims, strides, box);
+}
+
 // SwiGLU gate and up stacks w1, w3 (both bf16 [rows, cols], rows % 64 == 0)
 // as one 5-D tensor (64 columns, 64 rows, {first, second} stack, 64-row
 // blocks, cols / 64 chunks) whose third dimension steps between the two
@@ -833,8 +859,6 @@ struct BwdWs {
   float* du_router;                      // [T, H]
   float* cent_part;                      // [splits, E, H]
   __nv_bfloat16 *dx_perm, *dx_sh;        // [Tk, H], [Ks·T, H]
-  __nv_bfloat16 *w2t, *sw2t;             // [E, I, H], [Ks, I, H]
-  __nv_bfloat16 *w13t, *sw13t;           // [E, H, P·I], [Ks, H, P·I]
   int32_t* seg_start;                    // [E + 1]
   GroupDesc *wg2, *wg13;
   int4 *wk2, *wk13;
@@ -905,10 +929,6 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.cent_part = static_cast<float*>(take(static_cast<size_t>(cent_splits(s)) * E * H * 4));
   B.dx_perm = bf(Tk * H);
   B.dx_sh = bf(Ks * T * H);
-  B.w2t = bf(E * I * H);
-  B.sw2t = bf(Ks * I * H);
-  B.w13t = bf(E * H * P * I);
-  B.sw13t = bf(Ks * H * P * I);
   B.seg_start = static_cast<int32_t*>(take((E + 1) * 4));
   const size_t G2 = E + Ks, G13 = (E + Ks) * P;
   B.wg2 = static_cast<GroupDesc*>(take(G2 * sizeof(GroupDesc)));
@@ -937,23 +957,6 @@ MOE_API size_t moe_layer_backward_workspace_size(const moe_shape* s) {
   return check_backward(s) == MOE_OK ? carve_bwd(nullptr, s).total : 0;
 }
 
-// Batched transpose of `batch` bf16 matrices [R, C] (R, C % 64 == 0) into
-// dst [C, ...] at column col0 (row pitch dst_ld).
-moe_status transpose_weights(const void* src, int R, int C, int batch, __nv_bfloat16* dst,
-                             long long dst_ld, long long col0, long long dst_bstride,
-                             cudaStream_t st) {
-  if (batch == 0) return MOE_OK;
-  // 16-byte vectors on both sides
-  if (R % 64 || C % 64 || dst_ld % 8 || col0 % 8 || dst_bstride % 8 || !al16(src) || !al16(dst))
-    return MOE_ERR_INVALID_ARG;
-  dim3 grid(R / 64, C / 64, batch);
-  transpose_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
-                                         static_cast<long long>(R) * C, C, R, nullptr, nullptr, 0,
-                                         dst, dst_ld, col0, dst_bstride, 0);
-  MOE_CUDA(cudaGetLastError());
-  return MOE_OK;
-}
-
 // Token rows into the chunk-major K-major weight-gradient operands (cols
 // rows of features): rows [0, n) of src (row pitch = cols) into dst columns
 // [col0, col0 + roundup(n, 64)), zeros past n; with seg_start, the routed
@@ -964,8 +967,7 @@ moe_status transpose_rows(const __nv_bfloat16* src, int cols, int n, const int32
   if (max_cols <= 0) return MOE_OK;
   if (cols % 64 || col0 % 64 || !al16(src) || !al16(dst)) return MOE_ERR_INVALID_ARG;
   dim3 grid(cdiv(max_cols, 64), cols / 64, 1);
-  transpose_kernel<<<grid, 256, 0, st>>>(src, cols, 0, cols, n, seg_start, offsets, E, dst,
-                                         0, col0, 0, cols);
+  transpose_kernel<<<grid, 256, 0, st>>>(src, cols, n, seg_start, offsets, E, dst, col0);
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -1028,28 +1030,29 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
                                                    by_load, B.g1, B.g2, B.tile_prefix);
   MOE_CUDA(cudaGetLastError());
 
-  // ---- K-major weights for the input-gradient GEMMs
   const long long PI = static_cast<long long>(P) * I;
   if (Rall > 0) {
-  MOE_TRY(transpose_weights(wt->w2, H, I, E, B.w2t, H, 0, static_cast<long long>(I) * H, st));
-  MOE_TRY(transpose_weights(wt->w1, I, H, E, B.w13t, PI, 0, H * PI, st));
-  if (swiglu) MOE_TRY(transpose_weights(wt->w3, I, H, E, B.w13t, PI, I, H * PI, st));
-  if (Ks > 0) {
-    MOE_TRY(transpose_weights(wt->sw2, H, I, Ks, B.sw2t, H, 0, static_cast<long long>(I) * H, st));
-    MOE_TRY(transpose_weights(wt->sw1, I, H, Ks, B.sw13t, PI, 0, H * PI, st));
-    if (swiglu) MOE_TRY(transpose_weights(wt->sw3, I, H, Ks, B.sw13t, PI, I, H * PI, st));
-  }
-
   // ---- grouped GEMMs over the forward's groups: pre-activations and dm = dh W2
-  auto row_gemm = [&](const void* wr, const void* wsh, uint64_t rows_per_expert, int K,
+  // mn: the weights are stored as the operand's transpose ([K rows, M
+  // columns] per expert) and read MN-major
+  auto row_gemm = [&](const void* wr, const void* wsh, uint64_t rows_per_expert, int K, bool mn,
                       const void* b_routed, const void* b_shared, int b_shared_rows,
                       const GroupDesc* groups, void* out0, uint64_t out0_rows, void* out1,
                       uint64_t out1_rows, int out_cols) -> moe_status {
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3(&p.a[0], wr, static_cast<uint64_t>(E) * rows_per_expert, K, tc::kBM));
-    if (Ks) MOE_TRY(make_map3(&p.a[1], wsh, static_cast<uint64_t>(Ks) * rows_per_expert, K, tc::kBM));
-    else p.a[1] = p.a[0];
+    if (mn) {
+      MOE_TRY(make_map3_mn(&p.a[0], wr, static_cast<uint64_t>(E) * K, rows_per_expert));
+      if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wsh, static_cast<uint64_t>(Ks) * K, rows_per_expert));
+      else p.a[1] = p.a[0];
+      p.a_mn = 1;
+      p.a_mn_per_expert = static_cast<int>(rows_per_expert);
+      p.a_k_per_expert = K;
+    } else {
+      MOE_TRY(make_map3(&p.a[0], wr, static_cast<uint64_t>(E) * rows_per_expert, K, tc::kBM));
+      if (Ks) MOE_TRY(make_map3(&p.a[1], wsh, static_cast<uint64_t>(Ks) * rows_per_expert, K, tc::kBM));
+      else p.a[1] = p.a[0];
+    }
     MOE_TRY(make_token_maps(p.b[1], b_shared, b_shared_rows, K));
     if (b_routed != nullptr) MOE_TRY(make_token_maps(p.b[0], b_routed, Tk, K));
     else memcpy(p.b[0], p.b[1], sizeof(p.b[0]));
@@ -1068,9 +1071,11 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   };
   const void* xr = Tk > 0 ? B.x_perm : nullptr;
   const void* dr = Tk > 0 ? B.d_perm : nullptr;
-  MOE_TRY(row_gemm(wt->w1, wt->sw1, I, H, xr, u, T, B.g1, B.a, Rall, B.a, Rall, I));
-  if (swiglu) MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
-  MOE_TRY(row_gemm(B.w2t, B.sw2t, I, H, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
+  MOE_TRY(row_gemm(wt->w1, wt->sw1, I, H, false, xr, u, T, B.g1, B.a, Rall, B.a, Rall, I));
+  if (swiglu)
+    MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, false, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
+  // dm = dh W2: W2 [H, I] per expert is the operand's transpose
+  MOE_TRY(row_gemm(wt->w2, wt->sw2, I, H, true, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
 
   // ---- activation derivative, gate-scaled activation, <dm, act> per routed row
   {
@@ -1124,11 +1129,30 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
 
   // ---- dx = dh1 [W1; W3] per expert row, then du
   if (Rall > 0) {
+    // dx = [da | dc] [W1; W3]: W1 and W3 [I, H] per expert are the operand's
+    // transpose, read MN-major, W1's k-chunks first
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3(&p.a[0], B.w13t, static_cast<uint64_t>(E) * H, PI, tc::kBM));
-    if (Ks) MOE_TRY(make_map3(&p.a[1], B.sw13t, static_cast<uint64_t>(Ks) * H, PI, tc::kBM));
-    else p.a[1] = p.a[0];
+    p.a_mn_per_expert = H;
+    p.a_k_per_expert = I;
+    if (swiglu) {
+      p.a_mn = 2;
+      p.a_stack_chunks = I / tc::kBK;
+      MOE_TRY(make_map4_mn_pair(&p.a[0], wt->w1, wt->w3, static_cast<uint64_t>(E) * I, H,
+                                &p.a_stack_swap[0]));
+      if (Ks)
+        MOE_TRY(make_map4_mn_pair(&p.a[1], wt->sw1, wt->sw3, static_cast<uint64_t>(Ks) * I, H,
+                                  &p.a_stack_swap[1]));
+      else {
+        p.a[1] = p.a[0];
+        p.a_stack_swap[1] = p.a_stack_swap[0];
+      }
+    } else {
+      p.a_mn = 1;
+      MOE_TRY(make_map3_mn(&p.a[0], wt->w1, static_cast<uint64_t>(E) * I, H));
+      if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H));
+      else p.a[1] = p.a[0];
+    }
     MOE_TRY(make_token_maps(p.b[0], B.dh1, Rall, PI));
     memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
     p.groups = B.g2;

@@ -79,6 +79,19 @@ enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
 
 struct Params {
   CUtensorMap a[2];              // weight stacks (routed, shared): 3-D, or 5-D for SwiGLU
+  // Weight operand layout.  0: K-major (the maps above are K-major).  1 or 2:
+  // MN-major — the weights are read in their stored layout as the transpose
+  // of the operand: expert e's operand element (m, k) lives at row
+  // e · a_k_per_expert + k, column m of a row-major stack, and the map is
+  // (64 columns, rows, column blocks of 64) [1], or for two stacks read one
+  // after the other along k (W1 then W3) (64 columns, rows, 2 stacks, column
+  // blocks) [2] with a_stack_chunks k-chunks per stack (a_stack_swap: the
+  // map's first stack is the second one in k order).
+  int a_mn;
+  int a_mn_per_expert;           // operand rows (M) per expert: a_row0 = e · this
+  int a_k_per_expert;
+  int a_stack_chunks;
+  int a_stack_swap[2];           // per weight stack (routed, shared)
   CUtensorMap b[2][kNumBoxes];   // token sources x box heights: 3-D
   const GroupDesc* groups;       // [n_groups], or null for one dense group
   const int* tile_prefix;        // [n_groups + 1] prefix sum of token tiles
@@ -239,6 +252,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 
 template <int PAIR>
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  if (PAIR == 1)
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
+template <int PAIR>
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, int c3, int c4,
                                             uint64_t policy) {
@@ -343,10 +375,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);               // 128-byte swizzle
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-// m is the MMA's full M (256 for a CTA pair).
-__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle.  The
+// tile is stored as slabs of 64 M-elements (128 bytes) x K rows; 8-row
+// groups along K are 1024 bytes apart (stride offset) and the slabs of
+// consecutive 64-element M blocks are `slab` bytes apart (leading offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t slab) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>(slab >> 4) << 16) |      // leading offset: next M slab
+         (static_cast<uint64_t>(1024 >> 4) << 32) |      // stride offset: next 8 K rows
+         (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, B K-major, A
+// K-major or (a_mn) MN-major.  m is the MMA's full M (256 for a CTA pair).
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
 }
 
 template <int PAIR>
@@ -447,6 +492,7 @@ __device__ __forceinline__ int box_index(int rows) {
 // One tile as seen by one CTA (of rank `rank` in its pair).
 struct Tile {
   int a_sel, a_row;      // weight stack and this CTA's first weight row
+  int a_base;            // the group's first weight row (a_row0)
   int b_src, b_row;      // token source and this CTA's first token row
   int b_rows;            // token rows this CTA's half of the MMA reads (multiple of 16)
   int b_box;             // box index: the copy lands 16 << b_box >= b_rows rows
@@ -495,6 +541,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   constexpr int kCols = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;  // output columns per CTA
   Tile tl;
   tl.a_sel = d.a_sel;
+  tl.a_base = d.a_row0;
   tl.a_row = d.a_row0 + (w * PAIR + rank) * kCols;
   tl.n_valid = min(th, d.count - n * th);
   tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
@@ -593,7 +640,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // bytes both CTAs' copies deliver to the leader's barrier per stage
         const uint32_t bytes =
             static_cast<uint32_t>(PAIR * kKPS) * (kABytes + static_cast<uint32_t>(b_land) * (kBK * 2));
-        const uint32_t idesc = idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma));
+        const uint32_t idesc =
+            idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma), p.a_mn != 0 ? 1u : 0u);
+        // MN-major weights: the expert, its first k row and this CTA's first
+        // 64-column block
+        const int a_e = p.a_mn ? tl.a_base / p.a_mn_per_expert : 0;
+        const int a_k0 = a_e * p.a_k_per_expert;
+        const int a_mb = p.a_mn ? (tl.a_row - tl.a_base) / 64 : 0;
         const CUtensorMap* bmap = &p.b[tl.b_src][tl.b_box];
         for (int kb = 0; kb < tl.nk; kb += kKPS) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1)) {
@@ -613,11 +666,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (PAIR == 2) fb = map_to_rank(fb, 0);
           // weights: both k-blocks in one copy (chunk kb and kb + 1)
           const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
-          if (EPI == EPI_SWIGLU)
+          if (EPI == EPI_SWIGLU) {
             tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), tl.ka0 + kb,
                               pol_a);
-          else
+          } else if (p.a_mn == 1) {
+            // 128 k rows x two 64-column blocks: [block][row][64]
+            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, a_k0 + (tl.ka0 + kb) * kBK, a_mb, pol_a);
+          } else if (p.a_mn == 2) {
+            const int c = tl.ka0 + kb;  // k-chunk pairs never straddle the two stacks
+            const int stack = (c >= p.a_stack_chunks) != (p.a_stack_swap[tl.a_sel] != 0) ? 1 : 0;
+            const int row = a_k0 + (c >= p.a_stack_chunks ? c - p.a_stack_chunks : c) * kBK;
+            tma_load_4d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, row, stack, a_mb, pol_a);
+          } else {
             tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, tl.ka0 + kb, pol_a);
+          }
           // tokens: both k-blocks in one copy
           tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, tl.kb0 + kb, pol_keep);
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -660,11 +722,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           // a chunk past the end of K was zero-filled: its MMAs add nothing
 #pragma unroll
           for (int c = 0; c < kKPS; ++c) {
-            const uint64_t da = sdesc_sw128(sa + c * kABytes);
+            // K-major A: k-block c is the c-th 16 KB block, a 16-element k
+            // step is 32 bytes along the row.  MN-major A: two slabs of
+            // kKPS * 64 rows x 128 bytes; k-block c starts 64 rows into each
+            // slab, a k step is 16 rows (2 KB).
+            const uint64_t da = p.a_mn ? sdesc_sw128_mn(sa + c * (kBK * 128), kKPS * kBK * 128)
+                                       : sdesc_sw128(sa + c * kABytes);
+            const uint32_t a_step = p.a_mn ? (kUmmaK * 128) >> 4 : 2;
             const uint64_t db = sdesc_sw128(sa + kKPS * kABytes + c * boff);
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              tc_mma<PAIR>(d_tmem, da + 2 * k, db + 2 * k, idesc, ((kb + c) | k) != 0);
+              tc_mma<PAIR>(d_tmem, da + a_step * k, db + 2 * k, idesc, ((kb + c) | k) != 0);
           }
           tc_commit_all<PAIR>(empty_bar(stage));  // frees the stage in both CTAs once read
           if (++stage == S) { stage = 0; phase ^= 1; }
