@@ -15,8 +15,8 @@
 //                          activation for dW2 and the per-row <dy, y> for the
 //                          gate gradient
 //   gate_backward_kernel   dL/dz from dL/dg through softmax or the normalised
-//                          sigmoid
-//   router_grad_kernel     dz · centroids and dzᵀ · u (fp32, CUDA cores)
+//                          sigmoid (dz · centroids and dzᵀ · u are grouped
+//                          GEMMs too)
 //   grad_combine_kernel    du = dh + Σ shared dx + Σ slot dx + router term
 //   wgrad_plan_kernel      padded per-expert segments and the weight-gradient
 //                          GEMMs' groups
@@ -169,7 +169,9 @@ __global__ void __launch_bounds__(256) row_gate_kernel(const int32_t* __restrict
 
 // ---------------------------------------------------------------- gate
 
-// dL/dz for one token per warp from dg[t, s] = dg_row[slot_row[t, s]]:
+// dL/dz for one token per warp from dg[t, s] = dg_row[slot_row[t, s]],
+// written in bf16 with row pitch ld (>= E, zeros past E) as the operand of
+// the router-gradient GEMMs:
 //   softmax (g = s for the chosen): dz_e = s_e (dg_e [e chosen] − Σ_s dg_s g_s)
 //   sigmoid (g = s / S over the chosen): dz_e = (dg_e − Σ_s dg_s g_s) / S ·
 //            s_e (1 − s_e) for chosen e, 0 otherwise.
@@ -179,7 +181,8 @@ template <int NPL>
 __global__ void __launch_bounds__(256) gate_backward_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ topk_w, const int32_t* __restrict__ slot_row,
-    const float* __restrict__ dg_row, int T, int E, int k, int gate, float* __restrict__ dz) {
+    const float* __restrict__ dg_row, int T, int E, int k, int gate, int ld,
+    __nv_bfloat16* __restrict__ dz) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -239,83 +242,13 @@ __global__ void __launch_bounds__(256) gate_backward_kernel(
           if (e == lane + 32 * i) out[i] = v;
       }
     }
-    float* o = dz + static_cast<size_t>(t) * E;
+    __nv_bfloat16* o = dz + static_cast<size_t>(t) * ld;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) o[e] = out[i];
+      if (e < E) o[e] = __float2bfloat16_rn(out[i]);
     }
-  }
-}
-
-// ---------------------------------------------------------------- router GEMMs
-
-// out[m, n] = Σ_k A(m, k) · B[k, n] in fp32, k ascending: A fp32 with
-// element (m, k) at a[m * sam + k * sak], B bf16 [K, N] row-major, out fp32
-// [M, N] row-major.  64 x 64 output tiles, 4 x 4 per thread, K in steps of 16.
-// Used for dz · centroids (A = dz, sam = E, sak = 1) and dzᵀ · u (sam = 1,
-// sak = E).  blockIdx.z splits K into gridDim.z ranges of k_chunk; split z
-// writes its partial sums to out + z · M · N (reduced by
-// split_reduce_kernel in split order).
-__global__ void __launch_bounds__(256) router_grad_kernel(const float* __restrict__ a,
-                                                          long long sam, long long sak,
-                                                          const __nv_bfloat16* __restrict__ b,
-                                                          int M, int N, int K, int k_chunk,
-                                                          float* __restrict__ out) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  const int k_begin = blockIdx.z * k_chunk, k_end = min(K, k_begin + k_chunk);
-  out += static_cast<size_t>(blockIdx.z) * M * N;
-  const bool k_inner = sak == 1;   // A rows contiguous along k: load along k
-  float acc[4][4] = {};
-  for (int k0 = k_begin; k0 < k_end; k0 += 16) {
-    for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-      const int kk = k_inner ? (i & 15) : (i >> 6);
-      const int mm = k_inner ? (i >> 4) : (i & 63);
-      const int m = m0 + mm, kx = k0 + kk;
-      As[kk][mm] = (m < M && kx < k_end) ? __ldg(a + m * sam + kx * sak) : 0.0f;
-      const int kb = i >> 6, nn = i & 63;
-      const int n = n0 + nn, kbx = k0 + kb;
-      Bs[kb][nn] = (n < N && kbx < k_end) ? __bfloat162float(b[static_cast<size_t>(kbx) * N + n]) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n < N) out[static_cast<size_t>(m) * N + n] = acc[i][j];
-    }
-  }
-}
-
-// out[i] = Σ_{z < splits} part[z · n + i], z ascending.
-__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part,
-                                                           int splits, long long n,
-                                                           float* __restrict__ out) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float acc = 0.0f;
-    for (int z = 0; z < splits; ++z) acc += part[z * n + i];
-    out[i] = acc;
+    for (int e = E + lane; e < ld; e += 32) o[e] = __float2bfloat16_rn(0.0f);
   }
 }
 

@@ -855,9 +855,9 @@ struct BwdWs {
   __nv_bfloat16 *a, *c, *dm, *actg;      // [Rall, I]
   __nv_bfloat16* dh1;                    // [Rall, P·I]
   float *row_gate, *dg_row;              // [Tk]
-  float* dz;                             // [T, E]
+  __nv_bfloat16* dz;                     // [T, Epad], zeros past E
+  int Epad;                              // E rounded up to 64
   float* du_router;                      // [T, H]
-  float* cent_part;                      // [splits, E, H]
   __nv_bfloat16 *dx_perm, *dx_sh;        // [Tk, H], [Ks·T, H]
   int32_t* seg_start;                    // [E + 1]
   GroupDesc *wg2, *wg13;
@@ -868,19 +868,6 @@ struct BwdWs {
   long long Tpad, KX, KA;
   size_t total;
 };
-
-// Splits of T for the centroid gradient: enough 64 x 64 tiles x splits for
-// about four waves, each split at least 256 tokens, at most kMaxCentSplits;
-// the result depends only on the shape (fixed summation order).
-constexpr int kMaxCentSplits = 32;
-
-int cent_splits(const moe_shape* s) {
-  const int tiles = cdiv(s->H, 64) * cdiv(s->n_routed, 64);
-  const int want = std::max(1, std::min(cdiv(4 * 148, tiles), cdiv(std::max(s->T, 1), 256)));
-  const int splits = std::min(want, kMaxCentSplits);
-  const int k_chunk = cdiv(cdiv(std::max(s->T, 1), splits), 16) * 16;
-  return cdiv(std::max(s->T, 1), k_chunk);
-}
 
 BwdWs carve_bwd(void* ws, const moe_shape* s) {
   const size_t T = s->T, E = s->n_routed, k = s->top_k, Ks = s->n_shared, H = s->H,
@@ -924,9 +911,9 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.dh1 = bf(Rall * P * I);
   B.row_gate = static_cast<float*>(take(Tk * 4));
   B.dg_row = static_cast<float*>(take(Tk * 4));
-  B.dz = static_cast<float*>(take(T * E * 4));
+  B.Epad = static_cast<int>((E + tc::kBK - 1) / tc::kBK * tc::kBK);
+  B.dz = bf(T * static_cast<size_t>(B.Epad));
   B.du_router = static_cast<float*>(take(T * H * 4));
-  B.cent_part = static_cast<float*>(take(static_cast<size_t>(cent_splits(s)) * E * H * 4));
   B.dx_perm = bf(Tk * H);
   B.dx_sh = bf(Ks * T * H);
   B.seg_start = static_cast<int32_t*>(take((E + 1) * 4));
@@ -1006,6 +993,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   }
   const int Tk = T * k;
   const long long Rall = static_cast<long long>(Tk) + static_cast<long long>(Ks) * T;
+  const int Epad = B.Epad;
 
   // ---- the forward's routing, recomputed
   const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
@@ -1098,7 +1086,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
 #define MOE_GATE_BWD(N)                                                                 \
   gate_backward_kernel<N><<<blocks, 256, 0, st>>>(B.logits, B.idx, B.w, B.slot_row, B.dg_row, \
-                                                  T, E, k, gate, B.dz)
+                                                  T, E, k, gate, Epad, B.dz)
     if (npl <= 1) MOE_GATE_BWD(1);
     else if (npl <= 2) MOE_GATE_BWD(2);
     else if (npl <= 4) MOE_GATE_BWD(4);
@@ -1107,24 +1095,46 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     else MOE_GATE_BWD(32);
 #undef MOE_GATE_BWD
     MOE_CUDA(cudaGetLastError());
-    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(T, 64), 1), 256, 0, st>>>(
-        B.dz, E, 1, static_cast<const __nv_bfloat16*>(wt->centroids), T, H, E, E, B.du_router);
-    MOE_CUDA(cudaGetLastError());
-    // dzᵀ u contracts over all T tokens: split T so the grid fills the GPU,
-    // then add the partial sums in split order
-    const int splits = cent_splits(s);
-    const int k_chunk = cdiv(cdiv(T, splits), 16) * 16;
-    router_grad_kernel<<<dim3(cdiv(H, 64), cdiv(E, 64), splits), 256, 0, st>>>(
-        B.dz, 1, E, static_cast<const __nv_bfloat16*>(u), E, H, T, k_chunk,
-        splits > 1 ? B.cent_part : gr->d_centroids);
-    MOE_CUDA(cudaGetLastError());
-    if (splits > 1) {
-      const long long n = static_cast<long long>(E) * H;
-      split_reduce_kernel<<<static_cast<int>(std::min<long long>(cdiv(static_cast<int>(n), 256),
-                                                                  num_sms() * 8)),
-                            256, 0, st>>>(B.cent_part, splits, n, gr->d_centroids);
-      MOE_CUDA(cudaGetLastError());
-    }
+    // du += dz · centroids: the centroids [E, H] are the operand's transpose
+    // (read MN-major), dz is the token operand, K = E (padded to Epad)
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    MOE_TRY(make_map3_mn(&p.a[0], wt->centroids, E, H));
+    p.a[1] = p.a[0];
+    p.a_mn = 1;
+    p.a_mn_per_expert = H;
+    p.a_k_per_expert = E;
+    MOE_TRY(make_token_maps(p.b[0], B.dz, T, Epad));
+    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.dense_count = T;
+    p.n_wtiles = cdiv(H, 256);
+    p.num_k_blocks = Epad / tc::kBK;
+    p.out[0] = p.out[1] = B.du_router;
+    p.out_ld = H;
+    p.out_cols = H;
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
+    // d_centroids = dzᵀ u: dz [T, Epad] read MN-major (M = experts), uᵀ from
+    // the chunk-major copy of the shared experts' operand (K = T, padded
+    // with zeros to Tpad); stored transposed into [E, H]
+    MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(u), H, T, nullptr, nullptr, 0,
+                           static_cast<int>(B.Tpad), B.xT, 0, st));
+    tc::Params q;
+    memset(&q, 0, sizeof(q));
+    MOE_TRY(make_map3_mn(&q.a[0], B.dz, T, Epad));
+    q.a[1] = q.a[0];
+    q.a_mn = 1;
+    q.a_mn_per_expert = Epad;
+    q.a_k_per_expert = T;
+    MOE_TRY(make_token_maps_chunked(q.b[0], B.xT, H, B.KX / 64));
+    memcpy(q.b[1], q.b[0], sizeof(q.b[0]));
+    q.dense_count = H;
+    q.n_wtiles = cdiv(Epad, 256);
+    q.num_k_blocks = static_cast<int>(B.Tpad / tc::kBK);
+    q.out[0] = q.out[1] = gr->d_centroids;
+    q.out_ld = H;
+    q.out_cols = E;
+    q.out_tr = 1;
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(q, INT_MAX, st)));
   }
 
   // ---- dx = dh1 [W1; W3] per expert row, then du
@@ -1183,8 +1193,6 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   MOE_CUDA(cudaGetLastError());
   const int rmax = static_cast<int>(B.KX - B.Tpad);
   const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
-  MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(u), H, T, nullptr, nullptr, 0,
-                         static_cast<int>(tpad), B.xT, 0, st));
   MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(dh), H, T, nullptr, nullptr, 0,
                          static_cast<int>(tpad), B.dT, 0, st));
   for (int j = 0; j < Ks; ++j) {

@@ -108,6 +108,7 @@ struct Params {
   void* out[4];
   int out_ld;                    // output row pitch in elements
   int out_cols;                  // valid output columns
+  int out_tr;                    // EPI_F32: store the transpose (out[col * out_ld + row])
   const float* col_offset;       // EPI_F32: per-column addend, may be null
   int up_first[2];               // SwiGLU, per stack: the 5-D map lands the up rows first
   CUtensorMap omap[2];           // bf16 outputs out[0], out[1]: 2-D, box 32 columns x 32 rows
@@ -828,9 +829,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const bool col_ok = cols_ok && col < p.out_cols;
           const float add =
               (p.col_offset != nullptr && col_ok) ? __ldg(p.col_offset + col) : 0.0f;
-          float* o = static_cast<float*>(p.out[tl.out_sel]) +
-                     static_cast<size_t>(tl.out_row + c0) * p.out_ld + col;
-          if (col_ok) {
+          if (col_ok && p.out_tr) {
+            // transposed: this lane's 32 token rows are 32 consecutive floats
+            float* o = static_cast<float*>(p.out[tl.out_sel]) +
+                       static_cast<size_t>(col) * p.out_ld + tl.out_row + c0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nrow) o[j] = tl.nk == 0 ? 0.0f : __uint_as_float(v[j]) + add;
+          } else if (col_ok) {
+            float* o = static_cast<float*>(p.out[tl.out_sel]) +
+                       static_cast<size_t>(tl.out_row + c0) * p.out_ld + col;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < nrow)
