@@ -454,7 +454,8 @@ def expert_ffn_backward(x: np.ndarray, w1: np.ndarray, w2: np.ndarray,
 
 def layer_backward(u: np.ndarray, dh: np.ndarray, centroids: np.ndarray,
                    z: np.ndarray, idx: np.ndarray, gate: str, routed: ExpertFn,
-                   shared: ExpertFn, n_routed: int, n_shared: int, act: str):
+                   shared: ExpertFn, n_routed: int, n_shared: int, act: str,
+                   experts: Optional[Sequence[int]] = None):
     """Gradients of L = Σ dh ⊙ h (h from :func:`layer_forward` with the gate
     weights of :func:`gate_weights`) for the fixed choice idx, float64.
 
@@ -464,7 +465,9 @@ def layer_backward(u: np.ndarray, dh: np.ndarray, centroids: np.ndarray,
       dg_{t,s} = <dh_t, FFN_{idx[t,s]}(u_t)>,  d e_i = Σ_t dz_{t,i} u_t.
     Returns dict(du, d_centroids, dg, dz, dw1, dw3, dw2 [E, ...] and the
     shared dsw1, dsw3, dsw2 [Ks, ...]); experts nobody chose get zeros;
-    dw3 / dsw3 are None for ReLU.
+    dw3 / dsw3 are None for ReLU.  ``experts`` (for large layers) evaluates
+    only those routed experts — every expert a given token chose must be
+    among them — and returns dw1 / dw3 / dw2 as dicts expert -> array.
     """
     u = np.asarray(u, np.float64)
     dh = np.asarray(dh, np.float64)
@@ -482,8 +485,13 @@ def layer_backward(u: np.ndarray, dh: np.ndarray, centroids: np.ndarray,
         out["dsw3"].append(dw3)
         out["dsw2"].append(dw2)
     dg = np.zeros((T, k))
-    dw1s, dw3s, dw2s = [None] * n_routed, [None] * n_routed, [None] * n_routed
-    for e in range(n_routed):
+    if experts is not None:
+        missing = set(np.unique(idx).tolist()) - set(int(e) for e in experts)
+        if missing:
+            raise ValueError(f"chosen experts not evaluated: {sorted(missing)[:5]}")
+    loop = range(n_routed) if experts is None else [int(e) for e in experts]
+    dw1s, dw3s, dw2s = {}, {}, {}
+    for e in loop:
         w1, w3, w2 = routed(e)
         tt, ss = np.nonzero(idx == e)
         x = u[tt]
@@ -494,9 +502,13 @@ def layer_backward(u: np.ndarray, dh: np.ndarray, centroids: np.ndarray,
     dz = gate_backward(z, idx, gate, dg)
     cents = np.asarray(centroids, np.float64)
     du += dz @ cents
-    out.update(du=du, d_centroids=dz.T @ u, dg=dg, dz=dz,
-               dw1=np.stack(dw1s), dw2=np.stack(dw2s),
-               dw3=None if act == RELU else np.stack(dw3s))
+    if experts is None:
+        stack = lambda d: np.stack([d[e] for e in range(n_routed)])
+        out.update(dw1=stack(dw1s), dw2=stack(dw2s),
+                   dw3=None if act == RELU else stack(dw3s))
+    else:
+        out.update(dw1=dw1s, dw2=dw2s, dw3=None if act == RELU else dw3s)
+    out.update(du=du, d_centroids=dz.T @ u, dg=dg, dz=dz)
     for key in ("dsw1", "dsw2", "dsw3"):
         vals = out[key]
         out[key] = None if (not vals or vals[0] is None) else np.stack(vals)

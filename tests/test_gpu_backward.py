@@ -146,3 +146,56 @@ def test_backward_rejects_unsupported_shapes():
     assert M.moe_layer_backward_workspace_size(bad) == 0
     odd = _shape("bwd_odd_inter", inter=192)
     assert M.moe_layer_backward_workspace_size(odd) == 0
+
+
+# Full-size page-shaped layers in the configuration the benchmark times:
+# (shape name, sampled tokens for du, sampled routed experts for dW).
+FULL = [("dsmoe16b_bf16", 12, 3), ("v3_prefill_bf16", 6, 3)]
+
+
+@pytest.mark.parametrize("name,n_tok,n_exp", FULL, ids=[f[0] for f in FULL])
+def test_layer_backward_full_size_sampled(name, n_tok, n_exp):
+    """du on sampled tokens (each token's gradient depends only on that
+    token), the weight gradients of sampled routed experts (over all the rows
+    that chose them) and of the first shared expert (over all tokens).  The
+    centroid gradient sums dz over every token, which needs every expert's
+    output for every token: it is checked on the small layers only."""
+    shape = W.SHAPES[name]
+    inp = W.make_inputs(shape, DEV, seed=0)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    du, g = run_backward(shape, inp, dh)
+    torch.cuda.synchronize()
+    z, idx = forward_routing(shape, inp)
+    routed, shared = expert_fns(inp)
+    rng = np.random.default_rng(0)
+    u, dh64, cents = np64(inp.u), np64(dh), np64(inp.centroids)
+    tol = TOL["bf16"]
+    # du on sampled tokens
+    rows = np.sort(rng.choice(shape.T, size=n_tok, replace=False))
+    ref = O.layer_backward(u[rows], dh64[rows], cents, z[rows], idx[rows], shape.gate, routed,
+                           shared, shape.n_routed, shape.n_shared, shape.act,
+                           experts=np.unique(idx[rows]))
+    assert_close(np64(du)[rows], ref["du"], tol, f"{name} du")
+    # weight gradients of sampled routed experts: every row that chose them
+    gw, _ = O.gate_weights(z, idx, shape.gate)
+    counts = np.bincount(idx.reshape(-1), minlength=shape.n_routed)
+    for e in rng.choice(np.nonzero(counts)[0], size=n_exp, replace=False):
+        tt, ss = np.nonzero(idx == e)
+        w1, w3, w2 = routed(int(e))
+        _, dw1, dw3, dw2 = O.expert_ffn_backward(u[tt], w1, w2, w3, shape.act,
+                                                 gw[tt, ss][:, None] * dh64[tt])
+        assert_close(np64(g["dw1"][e]), dw1, tol, f"{name} dw1[{e}]")
+        assert_close(np64(g["dw2"][e]), dw2, tol, f"{name} dw2[{e}]")
+        if dw3 is not None:
+            assert_close(np64(g["dw3"][e]), dw3, tol, f"{name} dw3[{e}]")
+    # the first shared expert: every token
+    w1, w3, w2 = shared(0)
+    _, dw1, dw3, dw2 = O.expert_ffn_backward(u, w1, w2, w3, shape.act, dh64)
+    assert_close(np64(g["dsw1"][0]), dw1, tol, f"{name} dsw1[0]")
+    assert_close(np64(g["dsw2"][0]), dw2, tol, f"{name} dsw2[0]")
+    if dw3 is not None:
+        assert_close(np64(g["dsw3"][0]), dw3, tol, f"{name} dsw3[0]")
+    del inp, du, g
+    torch.cuda.empty_cache()

@@ -223,3 +223,25 @@ def test_planted_backward_mistakes():
         L = _layer(rng, T=5, H=6, E=5, Ks=1, I=4, k=2, gate=gate, act=act)
         with pytest.raises(AssertionError):
             check_finite_differences(m, L, rng)
+
+
+def test_expert_subset_matches_full_evaluation():
+    """Evaluating only the chosen experts gives the same du and the same
+    per-expert gradients as evaluating all of them."""
+    rng = np.random.default_rng(21)
+    L = _layer(rng, T=6, H=6, E=7, Ks=1, I=4, k=2, gate=O.SIGMOID_BIAS, act=O.SWIGLU)
+    full = _grads(O, L)
+    used = np.unique(L["idx"])
+    z = L["u"] @ L["cents"].T
+    E = L["E"]
+    sub = O.layer_backward(L["u"], L["dh"], L["cents"], z, L["idx"], L["gate"],
+                           lambda e: tuple(L["ws"][e]), lambda j: tuple(L["ws"][E + j]),
+                           E, L["Ks"], L["act"], experts=used)
+    assert np.array_equal(sub["du"], full["du"])
+    for e in used:
+        for key in ("dw1", "dw3", "dw2"):
+            assert np.array_equal(sub[key][e], full[key][e])
+    with pytest.raises(ValueError):
+        O.layer_backward(L["u"], L["dh"], L["cents"], z, L["idx"], L["gate"],
+                         lambda e: tuple(L["ws"][e]), lambda j: tuple(L["ws"][E + j]),
+                         E, L["Ks"], L["act"], experts=used[1:])
