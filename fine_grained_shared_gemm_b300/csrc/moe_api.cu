@@ -114,11 +114,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 moe_status encode(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
                   const cuuint64_t* strides, const cuuint32_t* box,
-                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                  CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cuda_fail(cudaErrorNotSupported);
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+  CUresult r = enc(m, dtype, rank, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : cuda_fail(cudaErrorInvalidValue);
@@ -199,6 +200,16 @@ moe_status make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {32, 32};
   return encode(m, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// fp32 output [rows, cols] row-major for the epilogue's bulk stores: box of
+// 32 columns x 32 rows.
+moe_status make_out_map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, 32};
+  return encode(m, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
 // Token-source maps for every box height.
@@ -1112,6 +1123,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     p.out[0] = p.out[1] = B.du_router;
     p.out_ld = H;
     p.out_cols = H;
+    p.f32_tma = 1;
+    MOE_TRY(make_out_map_f32(&p.omap32[0], B.du_router, T, H));
+    p.omap32[1] = p.omap32[0];
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
     // d_centroids = dzᵀ u: dz [T, Epad] read MN-major (M = experts), uᵀ from
     // the chunk-major copy of the shared experts' operand (K = T, padded
@@ -1225,6 +1239,10 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     p.out[1] = Ks ? gr->dsw2 : gr->dw2;
     p.out_ld = I;
     p.out_cols = I;
+    p.f32_tma = 1;
+    MOE_TRY(make_out_map_f32(&p.omap32[0], p.out[0], static_cast<uint64_t>(E) * H, I));
+    MOE_TRY(make_out_map_f32(&p.omap32[1], p.out[1],
+                             static_cast<uint64_t>(Ks ? Ks : E) * H, I));
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
   }
   {  // dW1[e][i][h] = Σ_r da_r[i] · x_r[h], dW3 likewise with dc
@@ -1245,6 +1263,12 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     p.out[3] = (Ks && swiglu) ? gr->dsw3 : gr->dw1;
     p.out_ld = H;
     p.out_cols = H;
+    p.f32_tma = 1;
+    for (int o = 0; o < 4; ++o) {
+      const bool sh = o >= 2 && Ks;  // out[2], out[3] are the shared stacks when Ks > 0
+      MOE_TRY(make_out_map_f32(&p.omap32[o], p.out[o],
+                               static_cast<uint64_t>(sh ? Ks : E) * I, H));
+    }
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
   }
   return MOE_OK;

@@ -112,6 +112,10 @@ struct Params {
   const float* col_offset;       // EPI_F32: per-column addend, may be null
   int up_first[2];               // SwiGLU, per stack: the 5-D map lands the up rows first
   CUtensorMap omap[2];           // bf16 outputs out[0], out[1]: 2-D, box 32 columns x 32 rows
+  // EPI_F32 with f32_tma: fp32 outputs out[0..3] as 2-D maps, box 32 x 32;
+  // full 32-row chunks leave as bulk tensor stores
+  int f32_tma;
+  CUtensorMap omap32[4];
 };
 
 constexpr int kMaxGroups = 1024;
@@ -836,6 +840,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < nrow) o[j] = tl.nk == 0 ? 0.0f : __uint_as_float(v[j]) + add;
+          } else if (p.f32_tma && nrow == 32 && cols_ok && tl.out_col + q * 32 < p.out_cols) {
+            // one 32 x 32 box per chunk from this warp's staging tile (single
+            // buffer: the previous store must have read it); columns past
+            // out_cols are clipped by the tensor map
+            float* stg = buf;
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              stg[j * 32 + lane] = tl.nk == 0 ? 0.0f : __uint_as_float(v[j]) + add;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.omap32[tl.out_sel], smem_u32(stg), tl.out_col + q * 32,
+                           tl.out_row + c0);
+              bulk_commit();
+            }
           } else if (col_ok) {
             float* o = static_cast<float*>(p.out[tl.out_sel]) +
                        static_cast<size_t>(tl.out_row + c0) * p.out_ld + col;
