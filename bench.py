@@ -285,13 +285,46 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
     ms = sum(a.elapsed_time(b) for a, b in ev) / K
     flops = 2 * expert_flops(s) + 4 * s.T * E * H
     tf = flops / (ms / 1e3) / 1e12
-    del ws, g, grads
+    # training step: the forward that keeps routing and pre-activations, then
+    # the backward that reuses them (each call timed on its own, L2 flushed)
+    saved = M.alloc_workspace(M.moe_layer_saved_size(s), dev)
+    h = torch.empty_like(dh)
+    for _ in range(args.warmup):
+        M.moe_layer_forward_train(s, layer.wt, inp.u, h, saved, layer.ws_l)
+        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws, saved=saved)
+    torch.cuda.synchronize()
+    ev_f = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev_f[i][0].record()
+        M.moe_layer_forward_train(s, layer.wt, inp.u, h, saved, layer.ws_l)
+        ev_f[i][1].record()
+        flush.zero_()
+        ev_b[i][0].record()
+        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws, saved=saved)
+        ev_b[i][1].record()
+    torch.cuda.synchronize()
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code} in the training step")
+    f_ms = sum(a.elapsed_time(b) for a, b in ev_f) / K
+    b_ms = sum(a.elapsed_time(b) for a, b in ev_b) / K
+    step_flops = expert_flops(s) + 2 * s.T * E * H + flops
+    del ws, g, grads, saved
     return {"tokens_per_s": round(s.T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
             "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
             "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
             "gpu_launches": backward_launches(s) * K,
             "note": "recomputes routing and the gate/up pre-activations from u; "
-                    "weight gradients fp32"}
+                    "weight gradients fp32",
+            "training_step": {
+                "forward_train_ms": round(f_ms, 4), "backward_saved_ms": round(b_ms, 4),
+                "tokens_per_s": round(s.T / ((f_ms + b_ms) / 1e3), 1),
+                "tflops": round(step_flops / ((f_ms + b_ms) / 1e3) / 1e12, 1),
+                "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"}}
 
 
 def run_cuda(args):

@@ -488,9 +488,13 @@ int ffn_bn(const moe_shape* s) {
   return (avg > 48 || (s->n_shared > 0 && s->top_k == 0 && s->T > 64)) ? 256 : 64;
 }
 
+// save_a / save_c (bf16 layers, may be null): GEMM1 also stores the
+// pre-activations a = x W1ᵀ and (SwiGLU) c = x W3ᵀ, [act_rows, I] each, rows
+// laid out like the activation (routed rows, then each shared expert's T).
 moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* u,
                          const void* u_perm, const int32_t* offsets, void* y_perm,
-                         void* y_shared, void* ws, cudaStream_t st) {
+                         void* y_shared, void* ws, cudaStream_t st, void* save_a = nullptr,
+                         void* save_c = nullptr) {
   const int T = s->T, E = s->n_routed, Ks = s->n_shared, k = s->top_k, H = s->H,
             I = s->inter;
   const int G = static_cast<int>(ffn_groups(s)), Tk = T * k;
@@ -575,6 +579,13 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   p.omap[1] = p.omap[0];
   p.out_ld = I;
   p.out_cols = I;
+  if (save_a != nullptr) {
+    p.save = 1;
+    p.save_out[0] = save_a;
+    p.save_out[1] = swiglu ? save_c : save_a;
+    MOE_TRY(make_out_map(&p.save_map[0], save_a, rows_act, I));
+    MOE_TRY(make_out_map(&p.save_map[1], p.save_out[1], rows_act, I));
+  }
   if (swiglu) MOE_TRY(launch_ffn<tc::EPI_SWIGLU>(p, bn, st));
   else MOE_TRY(launch_ffn<tc::EPI_RELU>(p, bn, st));
 
@@ -671,9 +682,46 @@ moe_status copy_streams(CopyStreams* out) {
   return MOE_OK;
 }
 
+// What moe_layer_forward_train keeps for moe_layer_backward.
+struct SavedLayout {
+  float* logits;       // [T, E]
+  int32_t* idx;        // [T, k]
+  float* w;            // [T, k]
+  int32_t* offsets;    // [E + 1]
+  int32_t* row_token;  // [T·k]
+  int32_t* slot_row;   // [T·k]
+  void* x_perm;        // [T·k, H]
+  void* a;             // [T·(k + Ks), I]
+  void* c;             // [T·(k + Ks), I] (SwiGLU)
+  size_t total;
+};
+
+SavedLayout carve_saved(void* base_ptr, const moe_shape* s) {
+  const size_t T = s->T, E = s->n_routed, k = s->top_k, H = s->H, I = s->inter;
+  char* base = static_cast<char*>(base_ptr);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base + off;
+    off += align256(bytes);
+    return static_cast<void*>(p);
+  };
+  SavedLayout S;
+  S.logits = static_cast<float*>(take(T * E * 4));
+  S.idx = static_cast<int32_t*>(take(T * k * 4));
+  S.w = static_cast<float*>(take(T * k * 4));
+  S.offsets = static_cast<int32_t*>(take((E + 1) * 4));
+  S.row_token = static_cast<int32_t*>(take(T * k * 4));
+  S.slot_row = static_cast<int32_t*>(take(T * k * 4));
+  S.x_perm = take(T * k * H * 2);
+  S.a = take(act_rows(s) * I * 2);
+  S.c = s->act == MOE_ACT_SWIGLU ? take(act_rows(s) * I * 2) : nullptr;
+  S.total = off;
+  return S;
+}
+
 moe_status layer_forward(const moe_shape* s, const moe_weights* wt, const void* u, void* h,
                          const moe_route_outputs* ro, void* ws, size_t ws_bytes,
-                         cudaStream_t st) {
+                         cudaStream_t st, void* saved = nullptr) {
   MOE_TRY(check_shape(s));
   MOE_TRY(check_weights_ffn(s, wt));
   if (!ok_ptr(wt->centroids) || !ok_opt(wt->logit_offset) || !ok_opt(wt->select_bias))
@@ -689,12 +737,29 @@ moe_status layer_forward(const moe_shape* s, const moe_weights* wt, const void* 
   int32_t* idx = (ro && ro->topk_idx) ? ro->topk_idx : L.idx;
   float* w = (ro && ro->topk_w) ? ro->topk_w : L.w;
   int32_t* offsets = (ro && ro->expert_offsets) ? ro->expert_offsets : L.offsets;
+  int32_t* row_token = L.row_token;
+  int32_t* slot_row = L.slot_row;
+  void* u_perm = L.u_perm;
+  void *save_a = nullptr, *save_c = nullptr;
+  if (saved != nullptr) {  // training: routing, permuted rows and pre-activations are kept
+    SavedLayout S = carve_saved(saved, s);
+    logits = S.logits;
+    idx = S.idx;
+    w = S.w;
+    offsets = S.offsets;
+    row_token = S.row_token;
+    slot_row = S.slot_row;
+    u_perm = S.x_perm;
+    save_a = S.a;
+    save_c = S.c;
+  }
   const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
   MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, logits, st));
   MOE_TRY(do_route(s, logits, bias, idx, w, nullptr, st));
-  MOE_TRY(do_dispatch(s, idx, u, offsets, L.row_token, L.slot_row, L.u_perm, L.dispatch_ws, st));
-  MOE_TRY(do_expert_ffn(s, wt, u, L.u_perm, offsets, L.y_perm, L.y_shared, L.ffn_ws, st));
-  return do_combine(s, u, L.y_perm, L.y_shared, w, L.slot_row, h, st);
+  MOE_TRY(do_dispatch(s, idx, u, offsets, row_token, slot_row, u_perm, L.dispatch_ws, st));
+  MOE_TRY(do_expert_ffn(s, wt, u, u_perm, offsets, L.y_perm, L.y_shared, L.ffn_ws, st, save_a,
+                        save_c));
+  return do_combine(s, u, L.y_perm, L.y_shared, w, slot_row, h, st);
 }
 
 }  // namespace
@@ -971,8 +1036,9 @@ moe_status transpose_rows(const __nv_bfloat16* src, int cols, int n, const int32
 }
 
 moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void* u,
-                          const void* dh, void* du, const moe_weight_grads* gr, void* ws,
-                          size_t ws_bytes, cudaStream_t st) {
+                          const void* dh, void* du, const moe_weight_grads* gr,
+                          const void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                          cudaStream_t st) {
   MOE_TRY(check_backward(s));
   MOE_TRY(check_weights_ffn(s, wt));
   if (!ok_ptr(wt->centroids) || !ok_opt(wt->logit_offset) || !ok_opt(wt->select_bias))
@@ -986,9 +1052,23 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   if (Ks > 0 && (!ok_ptr(gr->dsw1) || !ok_ptr(gr->dsw2) || (swiglu && !ok_ptr(gr->dsw3))))
     return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!ok_ptr(u) || !ok_ptr(dh) || !ok_ptr(du))) return MOE_ERR_INVALID_ARG;
+  if (saved != nullptr && (!al16(saved) || saved_bytes < carve_saved(nullptr, s).total))
+    return MOE_ERR_INVALID_ARG;
   BwdWs B = carve_bwd(nullptr, s);
   if (ws == nullptr || !al16(ws) || ws_bytes < B.total) return MOE_ERR_WORKSPACE;
   B = carve_bwd(ws, s);
+  if (saved != nullptr) {  // the forward's routing, permuted rows and pre-activations
+    SavedLayout S = carve_saved(const_cast<void*>(saved), s);
+    B.logits = S.logits;
+    B.idx = S.idx;
+    B.w = S.w;
+    B.offsets = S.offsets;
+    B.row_token = S.row_token;
+    B.slot_row = S.slot_row;
+    B.x_perm = static_cast<__nv_bfloat16*>(S.x_perm);
+    B.a = static_cast<__nv_bfloat16*>(S.a);
+    B.c = static_cast<__nv_bfloat16*>(S.c);
+  }
   const size_t wsz = static_cast<size_t>(I) * H * 4;
   if (T == 0) {  // no tokens: every gradient is zero
     MOE_CUDA(cudaMemsetAsync(gr->d_centroids, 0, static_cast<size_t>(E) * H * 4, st));
@@ -1006,12 +1086,14 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   const long long Rall = static_cast<long long>(Tk) + static_cast<long long>(Ks) * T;
   const int Epad = B.Epad;
 
-  // ---- the forward's routing, recomputed
-  const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
-  MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, B.logits, st));
-  MOE_TRY(do_route(s, B.logits, bias, B.idx, B.w, nullptr, st));
-  MOE_TRY(do_dispatch(s, B.idx, u, B.offsets, B.row_token, B.slot_row, B.x_perm,
-                      B.dispatch_ws, st));
+  // ---- the forward's routing, recomputed unless saved
+  if (saved == nullptr) {
+    const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
+    MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, B.logits, st));
+    MOE_TRY(do_route(s, B.logits, bias, B.idx, B.w, nullptr, st));
+    MOE_TRY(do_dispatch(s, B.idx, u, B.offsets, B.row_token, B.slot_row, B.x_perm,
+                        B.dispatch_ws, st));
+  }
   if (Tk > 0) {
     const int blocks = std::max(1, std::min(cdiv(Tk, 8), num_sms() * 16));
     gather_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
@@ -1070,9 +1152,11 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   };
   const void* xr = Tk > 0 ? B.x_perm : nullptr;
   const void* dr = Tk > 0 ? B.d_perm : nullptr;
-  MOE_TRY(row_gemm(wt->w1, wt->sw1, I, H, false, xr, u, T, B.g1, B.a, Rall, B.a, Rall, I));
-  if (swiglu)
-    MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, false, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
+  if (saved == nullptr) {  // pre-activations, recomputed
+    MOE_TRY(row_gemm(wt->w1, wt->sw1, I, H, false, xr, u, T, B.g1, B.a, Rall, B.a, Rall, I));
+    if (swiglu)
+      MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, false, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
+  }
   // dm = dh W2: W2 [H, I] per expert is the operand's transpose
   MOE_TRY(row_gemm(wt->w2, wt->sw2, I, H, true, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
 
@@ -1276,15 +1360,32 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
 
 MOE_API moe_status moe_layer_backward(const moe_shape* s, const moe_weights* weights,
                                       const void* u, const void* dh, void* du,
-                                      const moe_weight_grads* grads, void* ws, size_t ws_bytes,
+                                      const moe_weight_grads* grads, const void* saved,
+                                      size_t saved_bytes, void* ws, size_t ws_bytes,
                                       moe_stream_t stream) {
-  return layer_backward(s, weights, u, dh, du, grads, ws, ws_bytes, cs(stream));
+  return layer_backward(s, weights, u, dh, du, grads, saved, saved_bytes, ws, ws_bytes,
+                        cs(stream));
 }
 
 MOE_API moe_status moe_layer_forward(const moe_shape* s, const moe_weights* weights,
                                      const void* u, void* h, const moe_route_outputs* route_out,
                                      void* ws, size_t ws_bytes, moe_stream_t stream) {
   return layer_forward(s, weights, u, h, route_out, ws, ws_bytes, cs(stream));
+}
+
+MOE_API size_t moe_layer_saved_size(const moe_shape* s) {
+  if (check_shape(s) != MOE_OK || s->dtype != MOE_DTYPE_BF16) return 0;
+  return carve_saved(nullptr, s).total;
+}
+
+MOE_API moe_status moe_layer_forward_train(const moe_shape* s, const moe_weights* weights,
+                                           const void* u, void* h, void* saved,
+                                           size_t saved_bytes, void* ws, size_t ws_bytes,
+                                           moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (s->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(saved) || saved_bytes < carve_saved(nullptr, s).total) return MOE_ERR_INVALID_ARG;
+  return layer_forward(s, weights, u, h, nullptr, ws, ws_bytes, cs(stream), saved);
 }
 
 MOE_API moe_status moe_layer_forward_host(const moe_shape* s, const moe_weights* weights,

@@ -116,6 +116,11 @@ struct Params {
   // full 32-row chunks leave as bulk tensor stores
   int f32_tma;
   CUtensorMap omap32[4];
+  // EPI_SWIGLU with save: also store the gate (save_out[0]) and up
+  // (save_out[1]) pre-activations in bf16, same rows and columns as out
+  int save;
+  void* save_out[2];
+  CUtensorMap save_map[2];
 };
 
 constexpr int kMaxGroups = 1024;
@@ -782,7 +787,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // tile in this warp's shared memory (two buffers, alternating; the
         // store issued two chunks ago must have read the buffer); a partial
         // chunk is stored from registers, so no box writes past the group.
-        auto emit = [&](auto value_of, int col_base) {
+        auto emit_to = [&](const CUtensorMap* map, void* base, auto value_of, int col_base) {
           if (!cols_ok) return;
           if (nrow == 32) {
             uint16_t* stg = reinterpret_cast<uint16_t*>(buf) + (n_stores & 1) * 1024;
@@ -794,19 +799,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&p.omap[tl.out_sel], smem_u32(stg), tl.out_col + col_base,
-                           tl.out_row + c0);
+              tma_store_2d(map, smem_u32(stg), tl.out_col + col_base, tl.out_row + c0);
               bulk_commit();
             }
             ++n_stores;
           } else {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) +
                                static_cast<size_t>(tl.out_row + c0) * p.out_ld + tl.out_col +
                                col_base + lane;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < nrow) o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(value_of(j));
           }
+        };
+        auto emit = [&](auto value_of, int col_base) {
+          emit_to(&p.omap[tl.out_sel], p.out[tl.out_sel], value_of, col_base);
         };
         if (EPI == EPI_SWIGLU) {
           // lanes 0..63 hold the gate rows and 64..127 the matching up rows
@@ -824,6 +831,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               const float g = __uint_as_float(v[j]);
               return __fdividef(g, 1.0f + __expf(-g)) * up[j * 33 + lane];
             }, (q & 1) * 32);
+            if (p.save) {  // the pre-activations too, for a later backward
+              emit_to(&p.save_map[0], p.save_out[0],
+                      [&](int j) { return __uint_as_float(v[j]); }, (q & 1) * 32);
+              emit_to(&p.save_map[1], p.save_out[1],
+                      [&](int j) { return up[j * 33 + lane]; }, (q & 1) * 32);
+            }
           }
           named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
@@ -871,6 +884,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const float x = __uint_as_float(v[j]);
             return EPI == EPI_RELU ? fmaxf(x, 0.0f) : x;
           }, q * 32);
+          if (EPI == EPI_RELU && p.save)  // the pre-activation too, for a later backward
+            emit_to(&p.save_map[0], p.save_out[0], [&](int j) { return __uint_as_float(v[j]); },
+                    q * 32);
         }
       }
       // this warp has read the accumulator: tell the leader's MMA issuer

@@ -82,7 +82,10 @@ _SIGNATURES = {
     "moe_balance_stats_workspace_size": (ctypes.c_size_t, [_S]),
     "moe_layer_backward_workspace_size": (ctypes.c_size_t, [_S]),
     "moe_layer_backward": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.POINTER(moe_weight_grads),
-                                          _P, ctypes.c_size_t, _P]),
+                                          _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]),
+    "moe_layer_saved_size": (ctypes.c_size_t, [_S]),
+    "moe_layer_forward_train": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.c_size_t, _P,
+                                               ctypes.c_size_t, _P]),
     "moe_balance_stats": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -256,13 +259,29 @@ def weight_grads(d_centroids, dw1, dw3, dw2, dsw1=None, dsw3=None, dsw2=None) ->
     return moe_weight_grads(*[_ptr(t) for t in (d_centroids, dw1, dw3, dw2, dsw1, dsw3, dsw2)])
 
 
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def moe_layer_backward(shape, weights: moe_weights, u, dh, du, grads: moe_weight_grads, ws,
-                       stream=None):
-    """du and the weight gradients of the layer for the upstream gradient dh."""
+                       saved=None, stream=None):
+    """du and the weight gradients of the layer for the upstream gradient dh
+    (saved: the buffer of moe_layer_forward_train, or None to recompute)."""
     _check("moe_layer_backward", lib().moe_layer_backward(
         ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u), _ptr(dh), _ptr(du),
-        ctypes.byref(grads), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        ctypes.byref(grads), _ptr(saved), _nbytes(saved), _ptr(ws), _nbytes(ws),
         _stream(stream)))
+
+
+def moe_layer_saved_size(shape) -> int:
+    return lib().moe_layer_saved_size(ctypes.byref(shape_struct(shape)))
+
+
+def moe_layer_forward_train(shape, weights: moe_weights, u, h, saved, ws, stream=None):
+    """moe_layer_forward that also fills `saved` for moe_layer_backward."""
+    _check("moe_layer_forward_train", lib().moe_layer_forward_train(
+        ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u), _ptr(h), _ptr(saved),
+        _nbytes(saved), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:

@@ -272,19 +272,40 @@ typedef struct {
  *   du_t = dh_t + Σ_j J_j^T dh_t + Σ_s g_{t,s} J_{idx}^T dh_t + Σ_i dz_{t,i} e_i,
  *   dg_{t,s} = <dh_t, FFN_{idx[t,s]}(u_t)>, dz = dL/dlogits through softmax
  *   (no renormalisation) or the normalised sigmoid, d e_i = Σ_t dz_{t,i} u_t.
- * The call recomputes the forward's routing and the experts' pre-activations
- * from u (nothing is saved between the two calls), so it needs only the
- * forward's inputs.  fp32 accumulation; the intermediates (pre-activations,
- * per-row gradients, transposed operands) are bf16, as in the forward.
- * bf16 layers only, with inter % 128 == 0 and (n_routed + n_shared) x (2 for
- * SwiGLU, else 1) <= 1024 (otherwise MOE_ERR_UNSUPPORTED).  T = 0 writes
- * zero gradients.  ws: moe_layer_backward_workspace_size bytes. */
+ * With saved == NULL the call recomputes the forward's routing and the
+ * experts' pre-activations from u, so it needs only the forward's inputs;
+ * with the `saved` buffer that moe_layer_forward_train filled for the same
+ * u and weights it reuses them instead (saved_bytes >= moe_layer_saved_size).
+ * fp32 accumulation; the intermediates (pre-activations, per-row gradients,
+ * transposed operands) are bf16, as in the forward.  bf16 layers only, with
+ * inter % 128 == 0 and (n_routed + n_shared) x (2 for SwiGLU, else 1) <= 1024
+ * (otherwise MOE_ERR_UNSUPPORTED).  T = 0 writes zero gradients.
+ * ws: moe_layer_backward_workspace_size bytes. */
 MOE_API size_t moe_layer_backward_workspace_size(const moe_shape* shape);
 MOE_API moe_status moe_layer_backward(const moe_shape* shape,
                                       const moe_weights* weights, const void* u,
                                       const void* dh, void* du,
-                                      const moe_weight_grads* grads, void* ws,
-                                      size_t ws_bytes, moe_stream_t stream);
+                                      const moe_weight_grads* grads,
+                                      const void* saved, size_t saved_bytes,
+                                      void* ws, size_t ws_bytes,
+                                      moe_stream_t stream);
+
+/* Training forward: moe_layer_forward (same result h, bitwise) that also
+ * keeps, in the caller's `saved` buffer (device, 16-byte aligned,
+ * moe_layer_saved_size bytes), what moe_layer_backward would otherwise
+ * recompute: the router logits, the choice and gate weights, the dispatch
+ * (offsets and permutation), the permuted token rows and the experts'
+ * pre-activations x W1ᵀ (and x W3ᵀ for SwiGLU) in bf16, written by the
+ * gate/up GEMM's epilogue next to the activation.  The buffer's layout is
+ * private to the library; it stays valid while u and the weights do.  bf16
+ * layers only (0 / MOE_ERR_UNSUPPORTED otherwise).  ws:
+ * moe_layer_workspace_size bytes. */
+MOE_API size_t moe_layer_saved_size(const moe_shape* shape);
+MOE_API moe_status moe_layer_forward_train(const moe_shape* shape,
+                                           const moe_weights* weights,
+                                           const void* u, void* h, void* saved,
+                                           size_t saved_bytes, void* ws,
+                                           size_t ws_bytes, moe_stream_t stream);
 
 /* moe_dispatch without a workspace argument, for callers that cannot
  * allocate device memory: a runtime whose allocator already owns all of the

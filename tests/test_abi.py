@@ -153,3 +153,25 @@ def test_balance_stats_rejects_bad_pointers_and_workspace():
         M.MOE_ERR_WORKSPACE
     assert L.moe_balance_stats(ctypes.byref(s), 256, 256, 256, 256, None, need, None) == \
         M.MOE_ERR_WORKSPACE
+
+
+def test_training_entry_points_reject_bad_arguments():
+    s = _shape()
+    L = M.lib()
+    need = L.moe_layer_saved_size(ctypes.byref(s))
+    assert need > 0 and need % 256 == 0
+    assert L.moe_layer_saved_size(ctypes.byref(_shape(dtype=0))) == 0   # fp32: not supported
+    w = M.moe_weights(256, None, None, 256, 256, 256, 256, 256, 256)
+    ws = L.moe_layer_workspace_size(ctypes.byref(s))
+    assert L.moe_layer_forward_train(ctypes.byref(s), ctypes.byref(w), 256, 256, None, need,
+                                     256, ws, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_forward_train(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, need - 1,
+                                     256, ws, None) == M.MOE_ERR_INVALID_ARG
+    g = M.moe_weight_grads(256, 256, 256, 256, 256, 256, 256)
+    bws = L.moe_layer_backward_workspace_size(ctypes.byref(s))
+    assert L.moe_layer_backward(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, ctypes.byref(g),
+                                258, need, 256, bws, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_backward(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, ctypes.byref(g),
+                                256, need - 1, 256, bws, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_backward(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, ctypes.byref(g),
+                                None, 0, 256, bws - 1, None) == M.MOE_ERR_WORKSPACE

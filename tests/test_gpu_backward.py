@@ -53,13 +53,13 @@ def grads_buffers(shape):
     return g
 
 
-def run_backward(shape, inp, dh):
+def run_backward(shape, inp, dh, saved=None):
     g = grads_buffers(shape)
     du = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
     ws = M.alloc_workspace(M.moe_layer_backward_workspace_size(shape), DEV)
     M.moe_layer_backward(shape, M.weights_struct(inp), inp.u, dh, du,
                          M.weight_grads(g["d_centroids"], g["dw1"], g["dw3"], g["dw2"],
-                                        g["dsw1"], g["dsw3"], g["dsw2"]), ws)
+                                        g["dsw1"], g["dsw3"], g["dsw2"]), ws, saved=saved)
     st, code = M.moe_device_status()
     assert st == M.MOE_OK, (st, code)
     return du, g
@@ -81,13 +81,24 @@ def oracle_backward(shape, inp, dh, z, idx):
                             routed, shared, shape.n_routed, shape.n_shared, shape.act)
 
 
+def forward_train(shape, inp):
+    """moe_layer_forward_train: h and the saved buffer."""
+    ws = M.alloc_workspace(M.moe_layer_workspace_size(shape), DEV)
+    saved = M.alloc_workspace(M.moe_layer_saved_size(shape), DEV)
+    h = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=DEV)
+    M.moe_layer_forward_train(shape, M.weights_struct(inp), inp.u, h, saved, ws)
+    return h, saved
+
+
+@pytest.mark.parametrize("mode", ["recompute", "saved"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
-def test_layer_backward_matches_oracle(shape):
+def test_layer_backward_matches_oracle(shape, mode):
     inp = W.make_inputs(shape, DEV, seed=0)
     gen = torch.Generator(device=DEV)
     gen.manual_seed(1)
     dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
-    du, g = run_backward(shape, inp, dh)
+    saved = forward_train(shape, inp)[1] if mode == "saved" else None
+    du, g = run_backward(shape, inp, dh, saved)
     torch.cuda.synchronize()
     z, idx = forward_routing(shape, inp)
     ref = oracle_backward(shape, inp, dh, z, idx)
@@ -199,3 +210,16 @@ def test_layer_backward_full_size_sampled(name, n_tok, n_exp):
         assert_close(np64(g["dsw3"][0]), dw3, tol, f"{name} dsw3[0]")
     del inp, du, g
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", SHAPES[:3], ids=lambda s: s.name)
+def test_training_forward_matches_forward(shape):
+    """The training forward gives the forward's h bit for bit."""
+    inp = W.make_inputs(shape, DEV, seed=3)
+    h_train, _ = forward_train(shape, inp)
+    ws = M.alloc_workspace(M.moe_layer_workspace_size(shape), DEV)
+    h = torch.empty_like(h_train)
+    M.moe_layer_forward(shape, M.weights_struct(inp), inp.u, h, ws)
+    torch.cuda.synchronize()
+    assert M.moe_device_status()[0] == M.MOE_OK
+    assert torch.equal(h, h_train)
