@@ -831,12 +831,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               const float g = __uint_as_float(v[j]);
               return __fdividef(g, 1.0f + __expf(-g)) * up[j * 33 + lane];
             }, (q & 1) * 32);
-            if (p.save) {  // the pre-activations too, for a later backward
+            if (p.save)  // the gate pre-activation too, for a later backward
               emit_to(&p.save_map[0], p.save_out[0],
                       [&](int j) { return __uint_as_float(v[j]); }, (q & 1) * 32);
-              emit_to(&p.save_map[1], p.save_out[1],
-                      [&](int j) { return up[j * 33 + lane]; }, (q & 1) * 32);
-            }
+          } else if (p.save && cols_ok) {
+            // the up warp stores the up pre-activation it holds (same output
+            // columns as its partner's): 64 contiguous bytes per token row
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.save_out[1]) +
+                               static_cast<size_t>(tl.out_row + c0) * p.out_ld + tl.out_col +
+                               (q & 1) * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nrow)
+                o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
           named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
