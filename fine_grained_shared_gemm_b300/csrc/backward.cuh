@@ -11,9 +11,10 @@
 //   transpose_kernel       token rows into K-major operands for the weight
 //                          gradients, which contract over each expert's own
 //                          token rows (padded per expert to kSegAlign zeros)
-//   act_backward_kernel    SwiGLU / ReLU derivative per row, the gate-scaled
-//                          activation for dW2 and the per-row <dy, y> for the
-//                          gate gradient
+//   act_backward_kernel    SwiGLU / ReLU derivative per row, written row-major
+//                          and K-major, the gate-scaled activation (K-major,
+//                          for dW2) and the per-row <dy, y> for the gate
+//                          gradient
 //   gate_backward_kernel   dL/dz from dL/dg through softmax or the normalised
 //                          sigmoid (dz · centroids and dzᵀ · u are grouped
 //                          GEMMs too)
@@ -97,63 +98,119 @@ __global__ void __launch_bounds__(256) transpose_kernel(
 
 // ---------------------------------------------------------------- per-row derivative
 
-// Row r of the expert inputs (routed rows [0, Tk), then shared rows): with
-// a = x W1ᵀ, c = x W3ᵀ (SwiGLU) and dm = dh W2 for the row's token (the
-// upstream gradient NOT yet scaled by the gate weight g of the row; g = 1 for
-// shared rows):
-//   dg_row[r] = <dm, act>           act = SiLU(a) ⊙ c, or ReLU(a)   (r < Tk)
-//   dh1[r]    = [g dm ⊙ c ⊙ SiLU'(a) | g dm ⊙ SiLU(a)]   (SwiGLU, 2I wide)
-//             = g dm ⊙ [a > 0]                            (ReLU, I wide)
-//   actg[r]   = g act
-// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One warp per row, fp32 arithmetic on
-// the bf16 inputs; <dm, act> summed in a fixed order.
+// For row r of the expert inputs (routed rows [0, Tk), then shared rows) with
+// a = x W1ᵀ, c = x W3ᵀ (SwiGLU) and dm = dh W2 for the row's token (NOT yet
+// scaled by the row's gate weight g; g = 1 for shared rows):
+//   dh1[r]  = [g dm ⊙ c ⊙ SiLU'(a) | g dm ⊙ SiLU(a)]   (SwiGLU, 2I wide)
+//           = g dm ⊙ [a > 0]                            (ReLU, I wide)
+//   g act   with act = SiLU(a) ⊙ c, or ReLU(a)
+//   <dm, act> (= dL/dg of the row)
+// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One block per 64 rows x 64 features:
+// dh1 is written row-major (the input-gradient GEMM's operand) and, with g
+// act, also chunk-major K-major like transpose_kernel writes (the weight
+// gradients' operands: dh1ᵀ with P·I rows, (g act)ᵀ with I rows, column
+// col0 + j for row(j)); the 64 features' share of <dm, act> goes to
+// dg_part[r · (I / 64) + blockIdx.y] (routed rows only), summed later in
+// block order.  Rows come as in transpose_kernel: a run of rows_total rows
+// from row_base (seg_start == nullptr), or the routed rows in per-expert
+// segments; columns with no row get zeros.
 template <bool SWIGLU>
 __global__ void __launch_bounds__(256) act_backward_kernel(
     const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ c,
-    const __nv_bfloat16* __restrict__ dm, const float* __restrict__ row_gate, long long rows,
-    long long Tk, int I, __nv_bfloat16* __restrict__ dh1, __nv_bfloat16* __restrict__ actg,
-    float* __restrict__ dg_row) {
-  const int lane = threadIdx.x & 31;
-  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const int nvec = I / 8;
-  const int ld1 = SWIGLU ? 2 * I : I;
-  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       r < rows; r += warps) {
-    const float g = r < Tk ? __ldg(row_gate + r) : 1.0f;
+    const __nv_bfloat16* __restrict__ dm, const float* __restrict__ row_gate, long long Tk,
+    int I, long long row_base, int rows_total, const int32_t* __restrict__ seg_start,
+    const int32_t* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ dh1,
+    __nv_bfloat16* __restrict__ d1T, __nv_bfloat16* __restrict__ aT, long long col0,
+    float* __restrict__ dg_part) {
+  constexpr int P = SWIGLU ? 2 : 1;
+  __shared__ uint16_t t_da[64][66], t_dc[SWIGLU ? 64 : 1][66], t_ag[64][66];
+  const int j0 = blockIdx.x * 64;
+  const int f0 = blockIdx.y * 64;
+  const int nb = I / 64;
+  long long row0;
+  int valid;
+  if (seg_start == nullptr) {
+    row0 = row_base + j0;
+    valid = max(0, min(64, rows_total - j0));
+  } else {
+    if (j0 >= seg_start[E]) return;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seg_start[mid] <= j0) lo = mid; else hi = mid;
+    }
+    const int local = j0 - seg_start[lo];
+    row0 = offsets[lo] + local;
+    valid = max(0, min(64, offsets[lo + 1] - offsets[lo] - local));
+  }
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {   // two (row, 8 features) per thread
+    const int r = i >> 3, v = i & 7;
+    float da[8], dc[8], ag[8];
     float dot = 0.0f;
-    for (int v = lane; v < nvec; v += 32) {
-      const size_t off = static_cast<size_t>(r) * I + v * 8;
+    if (r < valid) {
+      const long long R = row0 + r;
+      const float g = R < Tk ? __ldg(row_gate + R) : 1.0f;
+      const size_t off = static_cast<size_t>(R) * I + f0 + v * 8;
       float fa[8], fc[8], fd[8];
       Vec16<__nv_bfloat16>::load(a + off, fa);
       Vec16<__nv_bfloat16>::load(dm + off, fd);
       if (SWIGLU) Vec16<__nv_bfloat16>::load(c + off, fc);
-      float o1[8], o2[8], o3[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int q = 0; q < 8; ++q) {
         if (SWIGLU) {
-          const float sg = 1.0f / (1.0f + expf(-fa[i]));
-          const float si = fa[i] * sg;
-          const float act = si * fc[i];
-          dot = fmaf(fd[i], act, dot);
-          const float gd = g * fd[i];
-          o1[i] = gd * fc[i] * sg * (1.0f + fa[i] * (1.0f - sg));
-          o2[i] = gd * si;
-          o3[i] = g * act;
+          const float sg = 1.0f / (1.0f + expf(-fa[q]));
+          const float si = fa[q] * sg;
+          const float act = si * fc[q];
+          dot = fmaf(fd[q], act, dot);
+          const float gd = g * fd[q];
+          da[q] = gd * fc[q] * sg * (1.0f + fa[q] * (1.0f - sg));
+          dc[q] = gd * si;
+          ag[q] = g * act;
         } else {
-          const float act = fmaxf(fa[i], 0.0f);
-          dot = fmaf(fd[i], act, dot);
-          o1[i] = fa[i] > 0.0f ? g * fd[i] : 0.0f;
-          o2[i] = 0.0f;
-          o3[i] = g * act;
+          const float act = fmaxf(fa[q], 0.0f);
+          dot = fmaf(fd[q], act, dot);
+          da[q] = fa[q] > 0.0f ? g * fd[q] : 0.0f;
+          dc[q] = 0.0f;
+          ag[q] = g * act;
         }
       }
-      const size_t off1 = static_cast<size_t>(r) * ld1 + v * 8;
-      Vec16<__nv_bfloat16>::store(dh1 + off1, o1);
-      if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1 + off1 + I, o2);
-      Vec16<__nv_bfloat16>::store(actg + off, o3);
+      const size_t off1 = static_cast<size_t>(R) * (P * I) + f0 + v * 8;
+      Vec16<__nv_bfloat16>::store(dh1 + off1, da);
+      if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1 + off1 + I, dc);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) da[q] = dc[q] = ag[q] = 0.0f;
     }
-    dot = warp_sum(dot);
-    if (lane == 0 && r < Tk) dg_row[r] = dot;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      t_da[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(da[q]));
+      if (SWIGLU) t_dc[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(dc[q]));
+      t_ag[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(ag[q]));
+    }
+    // the row's 8 vectors sit in 8 consecutive lanes: add them in a fixed order
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+    if (v == 0 && r < valid && row0 + r < Tk)
+      dg_part[static_cast<size_t>(row0 + r) * nb + blockIdx.y] = dot;
+  }
+  __syncthreads();
+  const size_t chunk = static_cast<size_t>((col0 + j0) >> 6);
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int f = i >> 3, v = i & 7;
+    uint4 xd, xc, xa;
+    uint16_t* hd = reinterpret_cast<uint16_t*>(&xd);
+    uint16_t* hc = reinterpret_cast<uint16_t*>(&xc);
+    uint16_t* ha = reinterpret_cast<uint16_t*>(&xa);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      hd[q] = t_da[v * 8 + q][f];
+      if (SWIGLU) hc[q] = t_dc[v * 8 + q][f];
+      ha[q] = t_ag[v * 8 + q][f];
+    }
+    *reinterpret_cast<uint4*>(d1T + (chunk * (P * I) + f0 + f) * 64 + v * 8) = xd;
+    if (SWIGLU) *reinterpret_cast<uint4*>(d1T + (chunk * (P * I) + I + f0 + f) * 64 + v * 8) = xc;
+    *reinterpret_cast<uint4*>(aT + (chunk * I + f0 + f) * 64 + v * 8) = xa;
   }
 }
 
@@ -169,7 +226,7 @@ __global__ void __launch_bounds__(256) row_gate_kernel(const int32_t* __restrict
 
 // ---------------------------------------------------------------- gate
 
-// dL/dz for one token per warp from dg[t, s] = dg_row[slot_row[t, s]],
+// dL/dz for one token per warp from dg[t, s] = Σ_b dg_part[slot_row[t, s], b],
 // written in bf16 with row pitch ld (>= E, zeros past E) as the operand of
 // the router-gradient GEMMs:
 //   softmax (g = s for the chosen): dz_e = s_e (dg_e [e chosen] − Σ_s dg_s g_s)
@@ -181,7 +238,7 @@ template <int NPL>
 __global__ void __launch_bounds__(256) gate_backward_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ topk_w, const int32_t* __restrict__ slot_row,
-    const float* __restrict__ dg_row, int T, int E, int k, int gate, int ld,
+    const float* __restrict__ dg_part, int n_parts, int T, int E, int k, int gate, int ld,
     __nv_bfloat16* __restrict__ dz) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -194,7 +251,8 @@ __global__ void __launch_bounds__(256) gate_backward_kernel(
       const size_t i = static_cast<size_t>(t) * k + lane;
       my_e = idx[i];
       my_g = topk_w[i];
-      my_dg = dg_row[slot_row[i]];
+      const float* part = dg_part + static_cast<size_t>(slot_row[i]) * n_parts;
+      for (int b = 0; b < n_parts; ++b) my_dg += part[b];   // feature blocks in order
       if (gate != 0) my_s = 1.0f / (1.0f + expf(-__ldg(z + my_e)));
     }
     const float cdot = warp_sum(my_dg * my_g);   // Σ_s dg_s g_s

@@ -928,9 +928,10 @@ struct BwdWs {
   GroupDesc* g2;
   int* tile_prefix;
   __nv_bfloat16 *x_perm, *d_perm;        // [Tk, H]
-  __nv_bfloat16 *a, *c, *dm, *actg;      // [Rall, I]
+  __nv_bfloat16 *a, *c, *dm;             // [Rall, I]
   __nv_bfloat16* dh1;                    // [Rall, P·I]
-  float *row_gate, *dg_row;              // [Tk]
+  float* row_gate;                       // [Tk]
+  float* dg_part;                        // [Tk, I / 64]: <dm, act> per 64-feature block
   __nv_bfloat16* dz;                     // [T, Epad], zeros past E
   int Epad;                              // E rounded up to 64
   float* du_router;                      // [T, H]
@@ -983,10 +984,9 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.a = bf(Rall * I);
   B.c = P == 2 ? bf(Rall * I) : nullptr;
   B.dm = bf(Rall * I);
-  B.actg = bf(Rall * I);
   B.dh1 = bf(Rall * P * I);
   B.row_gate = static_cast<float*>(take(Tk * 4));
-  B.dg_row = static_cast<float*>(take(Tk * 4));
+  B.dg_part = static_cast<float*>(take(Tk * (I / 64) * 4));
   B.Epad = static_cast<int>((E + tc::kBK - 1) / tc::kBK * tc::kBK);
   B.dz = bf(T * static_cast<size_t>(B.Epad));
   B.du_router = static_cast<float*>(take(T * H * 4));
@@ -1110,6 +1110,15 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
                                                    shared_pieces(s), shared_piece_rows(s),
                                                    by_load, B.g1, B.g2, B.tile_prefix);
   MOE_CUDA(cudaGetLastError());
+  // per-expert segments of the weight gradients' K-major operands and the
+  // weight-gradient GEMMs' groups
+  const int nt2 = cdiv(H, 256), nt13 = cdiv(I, 256);
+  wgrad_plan_kernel<<<1, 1024, 0, st>>>(B.offsets, E, Ks, static_cast<int>(B.Tpad), H, I, P,
+                                        B.seg_start, B.wg2, B.wk2, B.wg13, B.wk13, nt2, nt13,
+                                        B.wp2, B.wp13);
+  MOE_CUDA(cudaGetLastError());
+  const int rmax = static_cast<int>(B.KX - B.Tpad);
+  const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
 
   const long long PI = static_cast<long long>(P) * I;
   if (Rall > 0) {
@@ -1160,17 +1169,27 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   // dm = dh W2: W2 [H, I] per expert is the operand's transpose
   MOE_TRY(row_gemm(wt->w2, wt->sw2, I, H, true, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
 
-  // ---- activation derivative, gate-scaled activation, <dm, act> per routed row
+  // ---- activation derivative (row-major and K-major), gate-scaled
+  // activation (K-major), <dm, act> per routed row and 64-feature block
   {
-    const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>(
-        (Rall + 7) / 8, static_cast<long long>(num_sms()) * 16)));
-    if (swiglu)
-      act_backward_kernel<true><<<blocks, 256, 0, st>>>(B.a, B.c, B.dm, B.row_gate, Rall, Tk, I,
-                                                        B.dh1, B.actg, B.dg_row);
-    else
-      act_backward_kernel<false><<<blocks, 256, 0, st>>>(B.a, nullptr, B.dm, B.row_gate, Rall,
-                                                         Tk, I, B.dh1, B.actg, B.dg_row);
-    MOE_CUDA(cudaGetLastError());
+    auto act_bwd = [&](dim3 grid, long long row_base, int rows_total, const int32_t* seg,
+                       long long col0) -> moe_status {
+      if (swiglu)
+        act_backward_kernel<true><<<grid, 256, 0, st>>>(
+            B.a, B.c, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E, B.dh1,
+            B.d1T, B.aT, col0, B.dg_part);
+      else
+        act_backward_kernel<false><<<grid, 256, 0, st>>>(
+            B.a, nullptr, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
+            B.dh1, B.d1T, B.aT, col0, B.dg_part);
+      MOE_CUDA(cudaGetLastError());
+      return MOE_OK;
+    };
+    for (int j = 0; j < Ks; ++j)
+      MOE_TRY(act_bwd(dim3(static_cast<unsigned>(tpad / 64), I / 64), Tk + static_cast<long long>(j) * T,
+                      T, nullptr, j * tpad));
+    if (Tk > 0)
+      MOE_TRY(act_bwd(dim3(static_cast<unsigned>(cdiv(rmax, 64)), I / 64), 0, 0, B.seg_start, sh));
   }
 
   }  // Rall > 0
@@ -1180,8 +1199,8 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     const int npl = cdiv(E, 32);
     const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
 #define MOE_GATE_BWD(N)                                                                 \
-  gate_backward_kernel<N><<<blocks, 256, 0, st>>>(B.logits, B.idx, B.w, B.slot_row, B.dg_row, \
-                                                  T, E, k, gate, Epad, B.dz)
+  gate_backward_kernel<N><<<blocks, 256, 0, st>>>(B.logits, B.idx, B.w, B.slot_row, B.dg_part, \
+                                                  I / 64, T, E, k, gate, Epad, B.dz)
     if (npl <= 1) MOE_GATE_BWD(1);
     else if (npl <= 2) MOE_GATE_BWD(2);
     else if (npl <= 4) MOE_GATE_BWD(4);
@@ -1284,28 +1303,11 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   MOE_CUDA(cudaGetLastError());
 
   // ---- weight gradients: contractions over each expert's own rows
-  const int nt2 = cdiv(H, 256), nt13 = cdiv(I, 256);
-  wgrad_plan_kernel<<<1, 1024, 0, st>>>(B.offsets, E, Ks, static_cast<int>(B.Tpad), H, I, P,
-                                        B.seg_start, B.wg2, B.wk2, B.wg13, B.wk13, nt2, nt13,
-                                        B.wp2, B.wp13);
-  MOE_CUDA(cudaGetLastError());
-  const int rmax = static_cast<int>(B.KX - B.Tpad);
-  const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
   MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(dh), H, T, nullptr, nullptr, 0,
                          static_cast<int>(tpad), B.dT, 0, st));
-  for (int j = 0; j < Ks; ++j) {
-    const size_t r0 = static_cast<size_t>(Tk) + static_cast<size_t>(j) * T;
-    MOE_TRY(transpose_rows(B.actg + r0 * I, I, T, nullptr, nullptr, 0, static_cast<int>(tpad),
-                           B.aT, j * tpad, st));
-    MOE_TRY(transpose_rows(B.dh1 + r0 * PI, static_cast<int>(PI), T, nullptr, nullptr, 0,
-                           static_cast<int>(tpad), B.d1T, j * tpad, st));
-  }
   if (Tk > 0) {
     MOE_TRY(transpose_rows(B.x_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.xT, tpad, st));
     MOE_TRY(transpose_rows(B.d_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.dT, tpad, st));
-    MOE_TRY(transpose_rows(B.actg, I, Tk, B.seg_start, B.offsets, E, rmax, B.aT, sh, st));
-    MOE_TRY(transpose_rows(B.dh1, static_cast<int>(PI), Tk, B.seg_start, B.offsets, E, rmax,
-                           B.d1T, sh, st));
   }
   {  // dW2[e][h][i] = Σ_r dh_r[h] · (g act)_r[i]
     tc::Params p;
