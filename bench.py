@@ -234,17 +234,29 @@ class Layer:
         M.moe_combine(s, i.u, self.y_perm, self.y_shared, self.w, self.slot_row, self.h)
 
 
-def backward_launches(s: W.MoEShape) -> int:
-    """Kernel launches of one moe_layer_backward call (counted from its host code)."""
+def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
+    """Kernel launches of one moe_layer_backward call (counted from its host
+    code); saved: the call reuses moe_layer_forward_train's tensors."""
     sw = s.act == W.ACT_SWIGLU
-    n = 2 + (4 if s.top_k else 2)                 # logits, route, dispatch
-    n += 2 if s.top_k else 0                      # gather dh rows, row gate weights
-    n += 1                                        # FFN plan
-    n += 3 if sw else 2                           # pre-activations and dh W2
-    n += 1 + 1 + 2 + 1 + 1                        # act bwd, gate bwd, router grads, dx, du
-    n += 1 + 2 + 2 * s.n_shared + (4 if s.top_k else 0)  # plan, operand transposes
+    k = s.top_k > 0
+    n = 0
+    if not saved:
+        n += 2 + (4 if k else 1)                  # router logits, route, dispatch
+        n += 2 if sw else 1                       # pre-activations recomputed
+    n += 2 if k else 0                            # gather dh rows, row gate weights
+    n += 2                                        # FFN plan, weight-gradient plan
+    n += 1                                        # dm = dh W2
+    n += s.n_shared + (1 if k else 0)             # activation derivative
+    n += 1 + 3                                    # gate, router GEMMs + u transpose
+    n += 1 + 1                                    # dx, du
+    n += 1 + (2 if k else 0)                      # dh and routed x, dh transposes
     n += 2                                        # weight-gradient GEMMs
     return n
+
+
+def forward_launches(s: W.MoEShape) -> int:
+    """Kernel launches of one moe_layer_forward(_train) call."""
+    return 10 if s.top_k > 0 else 7
 
 
 def measure_backward(args, shape, layer, flush, dev, peaks):
@@ -322,6 +334,7 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
                     "weight gradients fp32",
             "training_step": {
                 "forward_train_ms": round(f_ms, 4), "backward_saved_ms": round(b_ms, 4),
+                "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
                 "tokens_per_s": round(s.T / ((f_ms + b_ms) / 1e3), 1),
                 "tflops": round(step_flops / ((f_ms + b_ms) / 1e3) / 1e12, 1),
                 "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"}}
