@@ -797,6 +797,14 @@ MOE_API moe_status moe_device_status(moe_stream_t stream, int32_t* code) {
   return MOE_OK;
 }
 
+MOE_API moe_status moe_check_bounded_wait(uint32_t limit_us, moe_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  tc::wait_timeout_probe_kernel<<<1, 32, 0, cs(stream)>>>(
+      static_cast<uint64_t>(limit_us) * 1000ull, DEV_ERR_TIMEOUT_MMA);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
 MOE_API size_t moe_dispatch_workspace_size(const moe_shape* s) {
   return check_shape(s) == MOE_OK ? dispatch_ws_bytes(s) : 0;
 }

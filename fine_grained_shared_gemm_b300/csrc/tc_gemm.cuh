@@ -230,15 +230,28 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Waits for the phase of the given parity to complete; false after the limit.
 template <bool kClusterScope = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
       if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Self-test of the bounded wait: one thread waits, with the GEMM's wait loop
+// and the given limit, on a barrier phase that nothing completes; when the
+// limit expires it sets `bits` in the device error word and returns.
+__global__ void __launch_bounds__(32) wait_timeout_probe_kernel(uint64_t limit_ns, int bits) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  if (!mbar_wait(b, 0, limit_ns)) raise_device_error(bits);
 }
 
 // Tiled TMA loads into this CTA's shared memory, with an L2 cache policy

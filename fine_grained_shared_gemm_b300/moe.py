@@ -84,6 +84,7 @@ _SIGNATURES = {
     "moe_layer_backward": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.POINTER(moe_weight_grads),
                                           _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]),
     "moe_layer_saved_size": (ctypes.c_size_t, [_S]),
+    "moe_check_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, _P]),
     "moe_layer_forward_train": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.c_size_t, _P,
                                                ctypes.c_size_t, _P]),
     "moe_balance_stats": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -271,6 +272,12 @@ def moe_layer_backward(shape, weights: moe_weights, u, dh, du, grads: moe_weight
         ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u), _ptr(dh), _ptr(du),
         ctypes.byref(grads), _ptr(saved), _nbytes(saved), _ptr(ws), _nbytes(ws),
         _stream(stream)))
+
+
+def moe_check_bounded_wait(limit_us: int, stream=None):
+    """Run the bounded-wait self-test (see include/moe.h); read the result with
+    moe_device_status()."""
+    _check("moe_check_bounded_wait", lib().moe_check_bounded_wait(limit_us, _stream(stream)))
 
 
 def moe_layer_saved_size(shape) -> int:

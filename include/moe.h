@@ -123,6 +123,15 @@ MOE_API int moe_last_cuda_error(void);
  * word was set, MOE_ERR_CUDA if the synchronisation failed, else MOE_OK. */
 MOE_API moe_status moe_device_status(moe_stream_t stream, int32_t* code);
 
+/* Self-test of failure detection: launches one thread that waits, with the
+ * same bounded barrier wait the grouped GEMM's roles use but a limit of
+ * limit_us microseconds (1..1000000), on a barrier phase that nothing
+ * completes.  The wait expires, the kernel sets the timeout bit of this
+ * device's error word and returns, so the next moe_device_status reports
+ * MOE_ERR_TIMEOUT and the context stays usable.  No GPU fault, trap or hang
+ * is involved. */
+MOE_API moe_status moe_check_bounded_wait(uint32_t limit_us, moe_stream_t stream);
+
 /* Scratch sizes in bytes (0 is a valid answer; an invalid shape returns 0). */
 MOE_API size_t moe_dispatch_workspace_size(const moe_shape* shape);
 MOE_API size_t moe_expert_ffn_workspace_size(const moe_shape* shape);

@@ -175,3 +175,9 @@ def test_training_entry_points_reject_bad_arguments():
                                 256, need - 1, 256, bws, None) == M.MOE_ERR_INVALID_ARG
     assert L.moe_layer_backward(ctypes.byref(s), ctypes.byref(w), 256, 256, 256, ctypes.byref(g),
                                 None, 0, 256, bws - 1, None) == M.MOE_ERR_WORKSPACE
+
+
+def test_bounded_wait_self_test_rejects_bad_limits():
+    L = M.lib()
+    assert L.moe_check_bounded_wait(0, None) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_check_bounded_wait(1000001, None) == M.MOE_ERR_INVALID_ARG
