@@ -40,6 +40,9 @@ SHAPES = [
            gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, logit_offset_std=3.0),
     _shape("bwd_shared_only", T=130, n_routed=4, n_shared=2, top_k=0, inter=128),
     _shape("bwd_one_token", T=1, n_routed=8, n_shared=1, top_k=2, inter=128),
+    # group-limited routing (V3 style): 32 experts in 8 groups, 3 groups kept
+    _shape("bwd_groups", T=400, n_routed=32, n_shared=1, top_k=4, inter=128,
+           gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, n_groups=8, topk_groups=3),
 ]
 
 
