@@ -226,3 +226,48 @@ def test_training_forward_matches_forward(shape):
     torch.cuda.synchronize()
     assert M.moe_device_status()[0] == M.MOE_OK
     assert torch.equal(h, h_train)
+
+
+def test_autograd_layer_matches_oracle():
+    """The torch.autograd wrapper: gradients of sum(h * dh) through a PyTorch
+    model equal the oracle's backward for the kernels' own choice."""
+    from fine_grained_shared_gemm_b300.autograd import MoELayer
+    shape = _shape("bwd_autograd", T=256, n_routed=8, n_shared=1, top_k=2, inter=128,
+                   gate=W.GATE_SIGMOID_BIAS)
+    layer = MoELayer(shape, DEV, seed=5)
+    with torch.no_grad():
+        layer.select_bias.uniform_(-0.1, 0.1)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(6)
+    u = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    u.requires_grad_(True)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    h = layer(u)
+    (h.float() * dh.float()).sum().backward()
+    torch.cuda.synchronize()
+    assert M.moe_device_status()[0] == M.MOE_OK
+    # the kernels' choice, from a plain forward of the same layer
+    T, E, k = shape.T, shape.n_routed, shape.top_k
+    ws = M.alloc_workspace(M.moe_layer_workspace_size(shape), DEV)
+    ro = dict(logits=torch.empty((T, E), dtype=torch.float32, device=DEV),
+              topk_idx=torch.empty((T, k), dtype=torch.int32, device=DEV))
+    h2 = torch.empty_like(h)
+    from fine_grained_shared_gemm_b300.autograd import _weights
+    wt = _weights(layer.centroids, layer.w1, layer.w3, layer.w2, layer.sw1, layer.sw3,
+                  layer.sw2, None, layer.select_bias)
+    M.moe_layer_forward(shape, wt, u.detach(), h2, ws, route_out=ro)
+    assert torch.equal(h.detach(), h2)
+    f = lambda t: np64(t.detach())
+    routed = lambda e: (f(layer.w1[e]), f(layer.w3[e]), f(layer.w2[e]))
+    shared = lambda j: (f(layer.sw1[j]), f(layer.sw3[j]), f(layer.sw2[j]))
+    ref = O.layer_backward(f(u), f(dh), f(layer.centroids), ro["logits"].cpu().numpy(),
+                           ro["topk_idx"].cpu().numpy().astype(np.int64), shape.gate, routed,
+                           shared, E, shape.n_shared, shape.act)
+    tol = TOL["bf16"]
+    assert_close(f(u.grad), ref["du"], tol, "du")
+    for name, key in (("centroids", "d_centroids"), ("w1", "dw1"), ("w3", "dw3"), ("w2", "dw2"),
+                      ("sw1", "dsw1"), ("sw3", "dsw3"), ("sw2", "dsw2")):
+        grad = getattr(layer, name).grad
+        assert grad is not None and grad.dtype == torch.bfloat16, name
+        # the parameter's bf16 gradient against the oracle (one more rounding)
+        assert_close(f(grad), ref[key], tol, name)
