@@ -9,14 +9,13 @@ fallback.
 from __future__ import annotations
 
 import ctypes
-import os
 import threading
 from typing import Optional
 
 import torch
 
 from . import _build
-from .workloads import ACT_SWIGLU, GATE_SOFTMAX, MoEInputs, MoEShape
+from .workloads import ACT_SWIGLU, GATE_SOFTMAX, MoEInputs
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1

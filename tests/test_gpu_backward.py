@@ -7,8 +7,6 @@ Every gradient tensor is compared element by element at sizes that span
 several tiles, ragged tails, experts that nobody chose, the shared-only and
 single-token cases; the bar is the layer's bf16 one, max|Δ| ≤ 2e-2 · max|ref|
 per tensor (the backward's intermediates are bf16 like the forward's)."""
-import dataclasses
-
 import numpy as np
 import pytest
 import torch
