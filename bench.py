@@ -80,6 +80,35 @@ def ffn_alg_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
     return (used * s.n_mats * s.H * s.inter + rows * s.H * 2 + rows * s.inter * 2) * e
 
 
+def ffn_roofline(shape: W.MoEShape, offsets: np.ndarray, ffn_s: float, peaks: dict) -> dict:
+    """The expert FFN's roofline entry for one launch of ffn_s seconds.
+
+    Decode-shaped layers (T·k < 2E) are timed against the HBM copy bandwidth
+    with the weights of every touched expert as the algorithmic bytes.  Other
+    layers are timed against their binding roof: the larger of the two lower
+    bounds, algorithmic FLOPs at the measured tensor peak and algorithmic
+    bytes at the measured copy bandwidth (the V3-shaped layer sits just on the
+    memory side of the ridge); the other roof is reported under other_roof.
+    """
+    flops = expert_flops(shape)
+    if shape.T * shape.top_k < 2 * shape.n_routed:
+        gb = touched_weight_bytes(shape, offsets) / ffn_s / 1e9
+        return {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4)}
+    alg_bytes = ffn_alg_bytes(shape, offsets)
+    t_flops = flops / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    tf = flops / ffn_s / 1e12
+    gb = alg_bytes / ffn_s / 1e9
+    tensor = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+              "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
+    memory = {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
+              "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4),
+              "algorithmic_bytes": alg_bytes}
+    roof, other = (memory, tensor) if t_bytes > t_flops else (tensor, memory)
+    return dict(roof, other_roof=other)
+
+
 def kernel_source_hash() -> str:
     src = os.path.join(ROOT, "fine_grained_shared_gemm_b300", "csrc", "tc_gemm.cuh")
     with open(src, "rb") as f:
@@ -254,12 +283,13 @@ def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
     if not saved:
         n += 2 + (4 if k else 1)                  # router logits, route, dispatch
         n += 2 if sw else 1                       # pre-activations recomputed
+    rows = k or s.n_shared > 0                    # any expert input rows at all
     n += 2 if k else 0                            # gather dh rows, row gate weights
     n += 2                                        # FFN plan, weight-gradient plan
-    n += 1                                        # dm = dh W2
+    n += 1 if rows else 0                         # dm = dh W2
     n += s.n_shared + (1 if k else 0)             # activation derivative
     n += 1 + 3                                    # gate, router GEMMs + u transpose
-    n += 1 + 1                                    # dx, du
+    n += (1 if rows else 0) + 1                   # dx, du
     n += 1 + (2 if k else 0)                      # dh and routed x, dh transposes
     n += 2                                        # weight-gradient GEMMs
     return n
@@ -414,29 +444,7 @@ def run_cuda(args):
     ffn_avg_s = sum(ffn_ms) / len(ffn_ms) / 1e3
     flops = expert_flops(shape)
     offsets = layer.off.cpu().numpy()
-    decode_like = shape.T * shape.top_k < 2 * shape.n_routed
-    if decode_like:
-        alg_bytes = touched_weight_bytes(shape, offsets)
-        achieved = alg_bytes / ffn_avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        # the binding roof of the expert FFN: the larger of its two lower
-        # bounds, algorithmic FLOPs at the measured tensor peak and
-        # algorithmic bytes at the measured copy bandwidth (the V3-shaped
-        # layer sits just on the memory side of the ridge)
-        alg_bytes = ffn_alg_bytes(shape, offsets)
-        t_flops = flops / (peaks["bf16_tflops"] * 1e12)
-        t_bytes = alg_bytes / (peaks["hbm_gbs"] * 1e9)
-        tf_ach = flops / ffn_avg_s / 1e12
-        gb_ach = alg_bytes / ffn_avg_s / 1e9
-        tensor = {"bound": "tensor", "achieved": round(tf_ach, 1), "peak": peaks["bf16_tflops"],
-                  "unit": "TFLOP/s", "frac": round(tf_ach / peaks["bf16_tflops"], 4)}
-        memory = {"bound": "hbm", "achieved": round(gb_ach, 1), "peak": peaks["hbm_gbs"],
-                  "unit": "GB/s", "frac": round(gb_ach / peaks["hbm_gbs"], 4),
-                  "algorithmic_bytes": alg_bytes}
-        roof, other = (memory, tensor) if t_bytes > t_flops else (tensor, memory)
-        roof = dict(roof, other_roof=other)
+    roof = ffn_roofline(shape, offsets, ffn_avg_s, peaks)
     roof.update({"traffic": recorded_traffic(args.workload), "kernel": "moe_expert_ffn",
                  "peak_source": f"{peak_src} (burst)", "ms_per_launch": round(ffn_avg_s * 1e3, 4)})
 
