@@ -279,11 +279,11 @@ def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
     code); saved: the call reuses moe_layer_forward_train's tensors."""
     sw = s.act == W.ACT_SWIGLU
     k = s.top_k > 0
+    rows = k or s.n_shared > 0                    # any expert input rows at all
     n = 0
     if not saved:
         n += 2 + (4 if k else 1)                  # router logits, route, dispatch
-        n += 2 if sw else 1                       # pre-activations recomputed
-    rows = k or s.n_shared > 0                    # any expert input rows at all
+        n += (2 if sw else 1) if rows else 0      # pre-activations recomputed
     n += 2 if k else 0                            # gather dh rows, row gate weights
     n += 2                                        # FFN plan, weight-gradient plan
     n += 1 if rows else 0                         # dm = dh W2

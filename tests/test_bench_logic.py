@@ -55,7 +55,7 @@ def test_backward_launch_counts():
     # no expert rows at all: no gathers, dm, derivative, dx or routed
     # transposes; dispatch is one scan when recomputing
     assert bench.backward_launches(relu, saved=True) == 2 + 4 + 1 + 1 + 2
-    assert bench.backward_launches(relu) == 2 + 4 + 1 + 1 + 2 + 3 + 1
+    assert bench.backward_launches(relu) == 2 + 4 + 1 + 1 + 2 + 3
     assert bench.forward_launches(s) == 10 and bench.forward_launches(relu) == 7
 
 
