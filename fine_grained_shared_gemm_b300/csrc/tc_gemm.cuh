@@ -838,11 +838,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]);
           }
           named_bar_sync(1, 128);
+          // the gate warps take the up values into registers, so that the
+          // hand-off area is free again at the second barrier and the up
+          // warps' next chunk overlaps this chunk's activation and stores
+          float upv[32];
           if (gate_warp) {
             const float* up = stage_buf + (q ^ 2) * 32 * 33;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) upv[j] = up[j * 33 + lane];
+          }
+          named_bar_sync(1, 128);
+          if (gate_warp) {
             emit([&](int j) {
               const float g = __uint_as_float(v[j]);
-              return __fdividef(g, 1.0f + __expf(-g)) * up[j * 33 + lane];
+              return __fdividef(g, 1.0f + __expf(-g)) * upv[j];
             }, (q & 1) * 32);
             if (p.save)  // the gate pre-activation too, for a later backward
               emit_to(&p.save_map[0], p.save_out[0],
@@ -858,7 +867,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               if (j < nrow)
                 o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
-          named_bar_sync(1, 128);
         } else if (EPI == EPI_F32) {
           // lane = output column: for each token row j the warp writes 32
           // consecutive fp32 columns (128 bytes) of that row
