@@ -32,8 +32,8 @@
  *    default stream) and returns without synchronising.  Arguments are
  *    checked on the host before anything is launched; a failed check
  *    launches nothing.  Errors are returned, never thrown.
- *  - The expert routing of one token never drops a token (no capacity
- *    factor; §4 "No token-dropping").
+ *  - The expert routing never drops a token (no capacity factor; the
+ *    page's §4 states that DeepSeekMoE drops none).
  *
  * Limits: 1 ≤ n_routed + n_shared ≤ 1024; 0 ≤ top_k ≤ min(32, n_routed);
  * H % 8 == 0 and inter % 8 == 0.  bf16 additionally needs H % 128 == 0 and
