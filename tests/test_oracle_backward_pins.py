@@ -245,3 +245,56 @@ def test_expert_subset_matches_full_evaluation():
         O.layer_backward(L["u"], L["dh"], L["cents"], z, L["idx"], L["gate"],
                          lambda e: tuple(L["ws"][e]), lambda j: tuple(L["ws"][E + j]),
                          E, L["Ks"], L["act"], experts=used[1:])
+
+
+def test_backward_hand_derived_single_token():
+    """One token u = (1, 2), centroids e0 = (1, 0), e1 = (0, 1): z = (1, 2),
+    softmax s = (1, e) / (1 + e), top-1 picks expert 1 with g = s1.  Expert 1
+    is ReLU with W1 = [1 1], W2 = [1 2]ᵀ: a = 3, y = (3, 6).  For dh = (1, 1):
+    dg = <dh, y> = 9; dz_1 = s1 (dg − dg s1) = 9 s1 s0, dz_0 = −9 s1 s0;
+    J = W2 W1 (a > 0), Jᵀ dh = (3, 3); du = dh + g Jᵀ dh + (dz_0, dz_1);
+    dm = W2ᵀ (g dh) = 3 g, dW1 = 3 g (1, 2), dW2 = (3 g, 3 g)ᵀ;
+    d e_i = dz_i (1, 2).  Expert 0 was not chosen: zero gradients."""
+    e = math.e
+    s1 = e / (1 + e)
+    s0 = 1 - s1
+    g = s1
+    u = np.array([[1.0, 2.0]])
+    dh = np.array([[1.0, 1.0]])
+    cents = np.array([[1.0, 0.0], [0.0, 1.0]])
+    W = {0: (np.array([[0.5, -0.5]]), None, np.array([[1.0], [1.0]])),
+         1: (np.array([[1.0, 1.0]]), None, np.array([[1.0], [2.0]]))}
+    z = u @ cents.T
+    idx = O.route(z.astype(np.float32), O.SOFTMAX, 1)["idx"]
+    assert idx.tolist() == [[1]]
+    G = O.layer_backward(u, dh, cents, z, idx, O.SOFTMAX, lambda k: W[k], lambda j: None,
+                         2, 0, O.RELU)
+    dz0, dz1 = -9 * s1 * s0, 9 * s1 * s0
+    assert np.allclose(G["dg"], [[9.0]], rtol=1e-14)
+    assert np.allclose(G["dz"], [[dz0, dz1]], rtol=1e-12)
+    assert np.allclose(G["du"], [[1 + 3 * g + dz0, 1 + 3 * g + dz1]], rtol=1e-12)
+    assert np.allclose(G["dw1"][1], [[3 * g, 6 * g]], rtol=1e-12)
+    assert np.allclose(G["dw2"][1], [[3 * g], [3 * g]], rtol=1e-12)
+    assert not G["dw1"][0].any() and not G["dw2"][0].any()
+    assert np.allclose(G["d_centroids"], [[dz0, 2 * dz0], [dz1, 2 * dz1]], rtol=1e-12)
+
+
+def test_backward_hand_derived_sigmoid_two_chosen():
+    """Sigmoid gate, both of two experts chosen, z = (0, 0): s = (1/2, 1/2),
+    g = s / Σ s = (1/2, 1/2).  Linear ReLU experts (positive pre-activation)
+    give y_0 = (1, 0), y_1 = (0, 3) for u = (1, 0), so for dh = (2, 1):
+    dg = (2, 3); ds_j = (dg_j − Σ_i dg_i g_i) / S = (−1/2, 1/2);
+    dz_j = ds_j s_j (1 − s_j) = (−1/8, 1/8)."""
+    u = np.array([[1.0, 0.0]])
+    dh = np.array([[2.0, 1.0]])
+    cents = np.zeros((2, 2))                       # z = 0 for both experts
+    W = {0: (np.array([[1.0, 0.0]]), None, np.array([[1.0], [0.0]])),
+         1: (np.array([[1.0, 0.0]]), None, np.array([[0.0], [3.0]]))}
+    z = u @ cents.T
+    idx = np.array([[0, 1]])
+    G = O.layer_backward(u, dh, cents, z, idx, O.SIGMOID_BIAS, lambda k: W[k], lambda j: None,
+                         2, 0, O.RELU)
+    assert np.allclose(G["dg"], [[2.0, 3.0]], rtol=1e-14)
+    assert np.allclose(G["dz"], [[-0.125, 0.125]], rtol=1e-14)
+    # du = dh + Σ_s g_s J_sᵀ dh + centroidsᵀ dz; J_0ᵀ dh = (2, 0), J_1ᵀ dh = (3, 0)
+    assert np.allclose(G["du"], [[2.0 + 0.5 * 2 + 0.5 * 3, 1.0]], rtol=1e-14)
