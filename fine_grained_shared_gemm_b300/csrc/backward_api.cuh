@@ -1,0 +1,465 @@
+// Host side of the layer backward: workspace layout, the launch sequence of
+// moe_layer_backward and its C entry points.  Included by moe_api.cu at the
+// point where the forward's host steps (tensor maps, launches, workspace
+// carving, the FFN plan) are already defined; not a stand-alone header.
+#pragma once
+
+// ---------------------------------------------------------------- backward
+
+// Workspace of the layer backward.  Rall = T·k + Ks·T expert input rows
+// (routed rows, then each shared expert's T rows); P = 2 (SwiGLU) or 1 (ReLU)
+// pre-activation blocks per row.  The weight-gradient operands are K-major
+// copies with the shared experts' T rows first (padded to Tpad) and then
+// each routed expert's rows (padded to kSegAlign).
+struct BwdWs {
+  float* logits;
+  int32_t* idx;
+  float* w;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* slot_row;
+  void* dispatch_ws;
+  GroupDesc* g1;
+  GroupDesc* g2;
+  int* tile_prefix;
+  __nv_bfloat16 *x_perm, *d_perm;        // [Tk, H]
+  __nv_bfloat16 *a, *c, *dm;             // [Rall, I]
+  __nv_bfloat16* dh1;                    // [Rall, P·I]
+  float* row_gate;                       // [Tk]
+  float* dg_part;                        // [Tk, I / 64]: <dm, act> per 64-feature block
+  __nv_bfloat16* dz;                     // [T, Epad], zeros past E
+  int Epad;                              // E rounded up to 64
+  float* du_router;                      // [T, H]
+  __nv_bfloat16 *dx_perm, *dx_sh;        // [Tk, H], [Ks·T, H]
+  int32_t* seg_start;                    // [E + 1]
+  GroupDesc *wg2, *wg13;
+  int4 *wk2, *wk13;
+  int *wp2, *wp13;
+  __nv_bfloat16 *xT, *dT;                // [H, KX]
+  __nv_bfloat16 *aT, *d1T;               // [I, KA], [P·I, KA]
+  long long Tpad, KX, KA;
+  size_t total;
+};
+
+BwdWs carve_bwd(void* ws, const moe_shape* s) {
+  const size_t T = s->T, E = s->n_routed, k = s->top_k, Ks = s->n_shared, H = s->H,
+               I = s->inter;
+  const size_t P = s->act == MOE_ACT_SWIGLU ? 2 : 1;
+  const size_t Tk = T * k, Rall = Tk + Ks * T;
+  const size_t Tpad = (T + kSegAlign - 1) / kSegAlign * kSegAlign;
+  // routed region: every expert's rows padded to kSegAlign; a multiple of
+  // kSegAlign itself, so row pitches stay 16-byte multiples and tensor maps
+  // cover whole k-chunks
+  const size_t Rmax = (Tk + kSegAlign - 1) / kSegAlign * kSegAlign + static_cast<size_t>(kSegAlign) * E;
+  char* base = static_cast<char*>(ws);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base + off;
+    off += align256(bytes);
+    return static_cast<void*>(p);
+  };
+  auto bf = [&](size_t n) { return static_cast<__nv_bfloat16*>(take(n * 2)); };
+  BwdWs B;
+  B.Tpad = static_cast<long long>(Tpad);
+  B.KX = static_cast<long long>(Tpad + Rmax);
+  B.KA = static_cast<long long>(Ks * Tpad + Rmax);
+  B.logits = static_cast<float*>(take(T * E * 4));
+  B.idx = static_cast<int32_t*>(take(Tk * 4));
+  B.w = static_cast<float*>(take(Tk * 4));
+  B.offsets = static_cast<int32_t*>(take((E + 1) * 4));
+  B.row_token = static_cast<int32_t*>(take(Tk * 4));
+  B.slot_row = static_cast<int32_t*>(take(Tk * 4));
+  B.dispatch_ws = take(dispatch_ws_bytes(s));
+  const size_t G = ffn_groups(s);
+  B.g1 = static_cast<GroupDesc*>(take(G * sizeof(GroupDesc)));
+  B.g2 = static_cast<GroupDesc*>(take(G * sizeof(GroupDesc)));
+  B.tile_prefix = static_cast<int*>(take((G + 1) * 4));
+  B.x_perm = bf(Tk * H);
+  B.d_perm = bf(Tk * H);
+  B.a = bf(Rall * I);
+  B.c = P == 2 ? bf(Rall * I) : nullptr;
+  B.dm = bf(Rall * I);
+  B.dh1 = bf(Rall * P * I);
+  B.row_gate = static_cast<float*>(take(Tk * 4));
+  B.dg_part = static_cast<float*>(take(Tk * (I / 64) * 4));
+  B.Epad = static_cast<int>((E + tc::kBK - 1) / tc::kBK * tc::kBK);
+  B.dz = bf(T * static_cast<size_t>(B.Epad));
+  B.du_router = static_cast<float*>(take(T * H * 4));
+  B.dx_perm = bf(Tk * H);
+  B.dx_sh = bf(Ks * T * H);
+  B.seg_start = static_cast<int32_t*>(take((E + 1) * 4));
+  const size_t G2 = E + Ks, G13 = (E + Ks) * P;
+  B.wg2 = static_cast<GroupDesc*>(take(G2 * sizeof(GroupDesc)));
+  B.wk2 = static_cast<int4*>(take(G2 * sizeof(int4)));
+  B.wp2 = static_cast<int*>(take((G2 + 1) * 4));
+  B.wg13 = static_cast<GroupDesc*>(take(G13 * sizeof(GroupDesc)));
+  B.wk13 = static_cast<int4*>(take(G13 * sizeof(int4)));
+  B.wp13 = static_cast<int*>(take((G13 + 1) * 4));
+  B.xT = bf(H * static_cast<size_t>(B.KX));
+  B.dT = bf(H * static_cast<size_t>(B.KX));
+  B.aT = bf(I * static_cast<size_t>(B.KA));
+  B.d1T = bf(P * I * static_cast<size_t>(B.KA));
+  B.total = off;
+  return B;
+}
+
+moe_status check_backward(const moe_shape* s) {
+  MOE_TRY(check_shape(s));
+  if (s->dtype != MOE_DTYPE_BF16 || s->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  const int P = s->act == MOE_ACT_SWIGLU ? 2 : 1;
+  if ((s->n_routed + s->n_shared) * P > tc::kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+MOE_API size_t moe_layer_backward_workspace_size(const moe_shape* s) {
+  return check_backward(s) == MOE_OK ? carve_bwd(nullptr, s).total : 0;
+}
+
+// Token rows into the chunk-major K-major weight-gradient operands (cols
+// rows of features): rows [0, n) of src (row pitch = cols) into dst columns
+// [col0, col0 + roundup(n, 64)), zeros past n; with seg_start, the routed
+// rows into per-expert segments.
+moe_status transpose_rows(const __nv_bfloat16* src, int cols, int n, const int32_t* seg_start,
+                          const int32_t* offsets, int E, int max_cols, __nv_bfloat16* dst,
+                          long long col0, cudaStream_t st) {
+  if (max_cols <= 0) return MOE_OK;
+  if (cols % 64 || col0 % 64 || !al16(src) || !al16(dst)) return MOE_ERR_INVALID_ARG;
+  dim3 grid(cdiv(max_cols, 64), cols / 64, 1);
+  transpose_kernel<<<grid, 256, 0, st>>>(src, cols, n, seg_start, offsets, E, dst, col0);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void* u,
+                          const void* dh, void* du, const moe_weight_grads* gr,
+                          const void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                          cudaStream_t st) {
+  MOE_TRY(check_backward(s));
+  MOE_TRY(check_weights_ffn(s, wt));
+  if (!ok_ptr(wt->centroids) || !ok_opt(wt->logit_offset) || !ok_opt(wt->select_bias))
+    return MOE_ERR_INVALID_ARG;
+  const bool swiglu = s->act == MOE_ACT_SWIGLU;
+  const int T = s->T, E = s->n_routed, Ks = s->n_shared, k = s->top_k, H = s->H, I = s->inter;
+  const int P = swiglu ? 2 : 1;
+  if (gr == nullptr || !ok_ptr(gr->d_centroids) || !ok_ptr(gr->dw1) || !ok_ptr(gr->dw2) ||
+      (swiglu && !ok_ptr(gr->dw3)))
+    return MOE_ERR_INVALID_ARG;
+  if (Ks > 0 && (!ok_ptr(gr->dsw1) || !ok_ptr(gr->dsw2) || (swiglu && !ok_ptr(gr->dsw3))))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ok_ptr(u) || !ok_ptr(dh) || !ok_ptr(du))) return MOE_ERR_INVALID_ARG;
+  if (saved != nullptr && (!al16(saved) || saved_bytes < carve_saved(nullptr, s).total))
+    return MOE_ERR_INVALID_ARG;
+  BwdWs B = carve_bwd(nullptr, s);
+  if (ws == nullptr || !al16(ws) || ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+  B = carve_bwd(ws, s);
+  if (saved != nullptr) {  // the forward's routing, permuted rows and pre-activations
+    SavedLayout S = carve_saved(const_cast<void*>(saved), s);
+    B.logits = S.logits;
+    B.idx = S.idx;
+    B.w = S.w;
+    B.offsets = S.offsets;
+    B.row_token = S.row_token;
+    B.slot_row = S.slot_row;
+    B.x_perm = static_cast<__nv_bfloat16*>(S.x_perm);
+    B.a = static_cast<__nv_bfloat16*>(S.a);
+    B.c = static_cast<__nv_bfloat16*>(S.c);
+  }
+  const size_t wsz = static_cast<size_t>(I) * H * 4;
+  if (T == 0) {  // no tokens: every gradient is zero
+    MOE_CUDA(cudaMemsetAsync(gr->d_centroids, 0, static_cast<size_t>(E) * H * 4, st));
+    MOE_CUDA(cudaMemsetAsync(gr->dw1, 0, E * wsz, st));
+    MOE_CUDA(cudaMemsetAsync(gr->dw2, 0, E * wsz, st));
+    if (swiglu) MOE_CUDA(cudaMemsetAsync(gr->dw3, 0, E * wsz, st));
+    if (Ks > 0) {
+      MOE_CUDA(cudaMemsetAsync(gr->dsw1, 0, Ks * wsz, st));
+      MOE_CUDA(cudaMemsetAsync(gr->dsw2, 0, Ks * wsz, st));
+      if (swiglu) MOE_CUDA(cudaMemsetAsync(gr->dsw3, 0, Ks * wsz, st));
+    }
+    return MOE_OK;
+  }
+  const int Tk = T * k;
+  const long long Rall = static_cast<long long>(Tk) + static_cast<long long>(Ks) * T;
+  const int Epad = B.Epad;
+
+  // ---- the forward's routing, recomputed unless saved
+  if (saved == nullptr) {
+    const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
+    MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, B.logits, st));
+    MOE_TRY(do_route(s, B.logits, bias, B.idx, B.w, nullptr, st));
+    MOE_TRY(do_dispatch(s, B.idx, u, B.offsets, B.row_token, B.slot_row, B.x_perm,
+                        B.dispatch_ws, st));
+  }
+  if (Tk > 0) {
+    const int blocks = std::max(1, std::min(cdiv(Tk, 8), num_sms() * 16));
+    gather_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(dh), T, B.row_token, B.offsets + E, H, B.d_perm);
+    MOE_CUDA(cudaGetLastError());
+    row_gate_kernel<<<cdiv(Tk, 256), 256, 0, st>>>(B.slot_row, B.w, Tk, B.row_gate);
+    MOE_CUDA(cudaGetLastError());
+  }
+  const int bn = ffn_bn(s);
+  const int pair = bn == 256 ? 2 : 1;
+  const int G = static_cast<int>(ffn_groups(s));
+  const int by_load = static_cast<long long>(Tk) <= 2LL * bn * E ? 1 : 0;
+  ffn_plan_kernel<<<1, cdiv(G, 32) * 32, 0, st>>>(B.offsets, E, Ks, T, Tk, I, H, bn,
+                                                   shared_pieces(s), shared_piece_rows(s),
+                                                   by_load, B.g1, B.g2, B.tile_prefix);
+  MOE_CUDA(cudaGetLastError());
+  // per-expert segments of the weight gradients' K-major operands and the
+  // weight-gradient GEMMs' groups
+  const int nt2 = cdiv(H, 256), nt13 = cdiv(I, 256);
+  wgrad_plan_kernel<<<1, 1024, 0, st>>>(B.offsets, E, Ks, static_cast<int>(B.Tpad), H, I, P,
+                                        B.seg_start, B.wg2, B.wk2, B.wg13, B.wk13, nt2, nt13,
+                                        B.wp2, B.wp13);
+  MOE_CUDA(cudaGetLastError());
+  const int rmax = static_cast<int>(B.KX - B.Tpad);
+  const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
+
+  const long long PI = static_cast<long long>(P) * I;
+  if (Rall > 0) {
+  // ---- grouped GEMMs over the forward's groups: pre-activations and dm = dh W2
+  // mn: the weights are stored as the operand's transpose ([K rows, M
+  // columns] per expert) and read MN-major
+  auto row_gemm = [&](const void* wr, const void* wsh, uint64_t rows_per_expert, int K, bool mn,
+                      const void* b_routed, const void* b_shared, int b_shared_rows,
+                      const GroupDesc* groups, void* out0, uint64_t out0_rows, void* out1,
+                      uint64_t out1_rows, int out_cols) -> moe_status {
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    if (mn) {
+      MOE_TRY(make_map3_mn(&p.a[0], wr, static_cast<uint64_t>(E) * K, rows_per_expert));
+      if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wsh, static_cast<uint64_t>(Ks) * K, rows_per_expert));
+      else p.a[1] = p.a[0];
+      p.a_mn = 1;
+      p.a_mn_per_expert = static_cast<int>(rows_per_expert);
+      p.a_k_per_expert = K;
+    } else {
+      MOE_TRY(make_map3(&p.a[0], wr, static_cast<uint64_t>(E) * rows_per_expert, K, tc::kBM));
+      if (Ks) MOE_TRY(make_map3(&p.a[1], wsh, static_cast<uint64_t>(Ks) * rows_per_expert, K, tc::kBM));
+      else p.a[1] = p.a[0];
+    }
+    MOE_TRY(make_token_maps(p.b[1], b_shared, b_shared_rows, K));
+    if (b_routed != nullptr) MOE_TRY(make_token_maps(p.b[0], b_routed, Tk, K));
+    else memcpy(p.b[0], p.b[1], sizeof(p.b[0]));
+    p.groups = groups;
+    p.tile_prefix = B.tile_prefix;
+    p.n_groups = G;
+    p.n_wtiles = cdiv(static_cast<int>(rows_per_expert), tc::kBM * pair);
+    p.num_k_blocks = cdiv(K, tc::kBK);
+    p.out[0] = out0;
+    p.out[1] = out1;
+    MOE_TRY(make_out_map(&p.omap[0], out0, out0_rows, out_cols));
+    MOE_TRY(make_out_map(&p.omap[1], out1, out1_rows, out_cols));
+    p.out_ld = out_cols;
+    p.out_cols = out_cols;
+    return launch_ffn<tc::EPI_BF16>(p, bn, st);
+  };
+  const void* xr = Tk > 0 ? B.x_perm : nullptr;
+  const void* dr = Tk > 0 ? B.d_perm : nullptr;
+  if (saved == nullptr) {  // pre-activations, recomputed
+    MOE_TRY(row_gemm(wt->w1, wt->sw1, I, H, false, xr, u, T, B.g1, B.a, Rall, B.a, Rall, I));
+    if (swiglu)
+      MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, false, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
+  }
+  // dm = dh W2: W2 [H, I] per expert is the operand's transpose
+  MOE_TRY(row_gemm(wt->w2, wt->sw2, I, H, true, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
+
+  // ---- activation derivative (row-major and K-major), gate-scaled
+  // activation (K-major), <dm, act> per routed row and 64-feature block
+  {
+    auto act_bwd = [&](dim3 grid, long long row_base, int rows_total, const int32_t* seg,
+                       long long col0) -> moe_status {
+      if (swiglu)
+        act_backward_kernel<true><<<grid, 256, 0, st>>>(
+            B.a, B.c, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E, B.dh1,
+            B.d1T, B.aT, col0, B.dg_part);
+      else
+        act_backward_kernel<false><<<grid, 256, 0, st>>>(
+            B.a, nullptr, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
+            B.dh1, B.d1T, B.aT, col0, B.dg_part);
+      MOE_CUDA(cudaGetLastError());
+      return MOE_OK;
+    };
+    for (int j = 0; j < Ks; ++j)
+      MOE_TRY(act_bwd(dim3(static_cast<unsigned>(tpad / 64), I / 64), Tk + static_cast<long long>(j) * T,
+                      T, nullptr, j * tpad));
+    if (Tk > 0)
+      MOE_TRY(act_bwd(dim3(static_cast<unsigned>(cdiv(rmax, 64)), I / 64), 0, 0, B.seg_start, sh));
+  }
+
+  }  // Rall > 0
+  // ---- gate gradient and the router's share of du and of the centroids
+  {
+    const int blocks = route_blocks(T);
+    const int npl = cdiv(E, 32);
+    const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
+#define MOE_GATE_BWD(N)                                                                 \
+  gate_backward_kernel<N><<<blocks, 256, 0, st>>>(B.logits, B.idx, B.w, B.slot_row, B.dg_part, \
+                                                  I / 64, T, E, k, gate, Epad, B.dz)
+    if (npl <= 1) MOE_GATE_BWD(1);
+    else if (npl <= 2) MOE_GATE_BWD(2);
+    else if (npl <= 4) MOE_GATE_BWD(4);
+    else if (npl <= 8) MOE_GATE_BWD(8);
+    else if (npl <= 16) MOE_GATE_BWD(16);
+    else MOE_GATE_BWD(32);
+#undef MOE_GATE_BWD
+    MOE_CUDA(cudaGetLastError());
+    // du += dz · centroids: the centroids [E, H] are the operand's transpose
+    // (read MN-major), dz is the token operand, K = E (padded to Epad)
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    MOE_TRY(make_map3_mn(&p.a[0], wt->centroids, E, H));
+    p.a[1] = p.a[0];
+    p.a_mn = 1;
+    p.a_mn_per_expert = H;
+    p.a_k_per_expert = E;
+    MOE_TRY(make_token_maps(p.b[0], B.dz, T, Epad));
+    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.dense_count = T;
+    p.n_wtiles = cdiv(H, 256);
+    p.num_k_blocks = Epad / tc::kBK;
+    p.out[0] = p.out[1] = B.du_router;
+    p.out_ld = H;
+    p.out_cols = H;
+    p.f32_tma = 1;
+    MOE_TRY(make_out_map_f32(&p.omap32[0], B.du_router, T, H));
+    p.omap32[1] = p.omap32[0];
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
+    // d_centroids = dzᵀ u: dz [T, Epad] read MN-major (M = experts), uᵀ from
+    // the chunk-major copy of the shared experts' operand (K = T, padded
+    // with zeros to Tpad); stored transposed into [E, H]
+    MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(u), H, T, nullptr, nullptr, 0,
+                           static_cast<int>(B.Tpad), B.xT, 0, st));
+    tc::Params q;
+    memset(&q, 0, sizeof(q));
+    MOE_TRY(make_map3_mn(&q.a[0], B.dz, T, Epad));
+    q.a[1] = q.a[0];
+    q.a_mn = 1;
+    q.a_mn_per_expert = Epad;
+    q.a_k_per_expert = T;
+    MOE_TRY(make_token_maps_chunked(q.b[0], B.xT, H, B.KX / 64));
+    memcpy(q.b[1], q.b[0], sizeof(q.b[0]));
+    q.dense_count = H;
+    q.n_wtiles = cdiv(Epad, 256);
+    q.num_k_blocks = static_cast<int>(B.Tpad / tc::kBK);
+    q.out[0] = q.out[1] = gr->d_centroids;
+    q.out_ld = H;
+    q.out_cols = E;
+    q.out_tr = 1;
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(q, INT_MAX, st)));
+  }
+
+  // ---- dx = dh1 [W1; W3] per expert row, then du
+  if (Rall > 0) {
+    // dx = [da | dc] [W1; W3]: W1 and W3 [I, H] per expert are the operand's
+    // transpose, read MN-major, W1's k-chunks first
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    p.a_mn_per_expert = H;
+    p.a_k_per_expert = I;
+    if (swiglu) {
+      p.a_mn = 2;
+      p.a_stack_chunks = I / tc::kBK;
+      MOE_TRY(make_map4_mn_pair(&p.a[0], wt->w1, wt->w3, static_cast<uint64_t>(E) * I, H,
+                                &p.a_stack_swap[0]));
+      if (Ks)
+        MOE_TRY(make_map4_mn_pair(&p.a[1], wt->sw1, wt->sw3, static_cast<uint64_t>(Ks) * I, H,
+                                  &p.a_stack_swap[1]));
+      else {
+        p.a[1] = p.a[0];
+        p.a_stack_swap[1] = p.a_stack_swap[0];
+      }
+    } else {
+      p.a_mn = 1;
+      MOE_TRY(make_map3_mn(&p.a[0], wt->w1, static_cast<uint64_t>(E) * I, H));
+      if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H));
+      else p.a[1] = p.a[0];
+    }
+    MOE_TRY(make_token_maps(p.b[0], B.dh1, Rall, PI));
+    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.groups = B.g2;
+    p.tile_prefix = B.tile_prefix;
+    p.n_groups = G;
+    p.n_wtiles = cdiv(H, tc::kBM * pair);
+    p.num_k_blocks = static_cast<int>(PI / tc::kBK);
+    void* o0 = Tk ? static_cast<void*>(B.dx_perm) : static_cast<void*>(B.dx_sh);
+    void* o1 = Ks ? static_cast<void*>(B.dx_sh) : static_cast<void*>(B.dx_perm);
+    p.out[0] = o0;
+    p.out[1] = o1;
+    MOE_TRY(make_out_map(&p.omap[0], o0, Tk ? Tk : static_cast<uint64_t>(Ks) * T, H));
+    MOE_TRY(make_out_map(&p.omap[1], o1, Ks ? static_cast<uint64_t>(Ks) * T : Tk, H));
+    p.out_ld = H;
+    p.out_cols = H;
+    MOE_TRY(launch_ffn<tc::EPI_BF16>(p, bn, st));
+  }
+  grad_combine_kernel<<<route_blocks(T), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(dh), B.dx_perm, B.dx_sh, B.slot_row, B.du_router, T, H,
+      k, Ks, static_cast<__nv_bfloat16*>(du));
+  MOE_CUDA(cudaGetLastError());
+
+  // ---- weight gradients: contractions over each expert's own rows
+  MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(dh), H, T, nullptr, nullptr, 0,
+                         static_cast<int>(tpad), B.dT, 0, st));
+  if (Tk > 0) {
+    MOE_TRY(transpose_rows(B.x_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.xT, tpad, st));
+    MOE_TRY(transpose_rows(B.d_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.dT, tpad, st));
+  }
+  {  // dW2[e][h][i] = Σ_r dh_r[h] · (g act)_r[i]
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    MOE_TRY(make_map3_chunked(&p.a[0], B.aT, I, B.KA / 64, tc::kBM));
+    p.a[1] = p.a[0];
+    MOE_TRY(make_token_maps_chunked(p.b[0], B.dT, H, B.KX / 64));
+    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.groups = B.wg2;
+    p.tile_prefix = B.wp2;
+    p.krange = B.wk2;
+    p.n_groups = E + Ks;
+    p.n_wtiles = cdiv(I, 256);
+    p.out[0] = gr->dw2;
+    p.out[1] = Ks ? gr->dsw2 : gr->dw2;
+    p.out_ld = I;
+    p.out_cols = I;
+    p.f32_tma = 1;
+    MOE_TRY(make_out_map_f32(&p.omap32[0], p.out[0], static_cast<uint64_t>(E) * H, I));
+    MOE_TRY(make_out_map_f32(&p.omap32[1], p.out[1],
+                             static_cast<uint64_t>(Ks ? Ks : E) * H, I));
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
+  }
+  {  // dW1[e][i][h] = Σ_r da_r[i] · x_r[h], dW3 likewise with dc
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    MOE_TRY(make_map3_chunked(&p.a[0], B.xT, H, B.KX / 64, tc::kBM));
+    p.a[1] = p.a[0];
+    MOE_TRY(make_token_maps_chunked(p.b[0], B.d1T, PI, B.KA / 64));
+    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.groups = B.wg13;
+    p.tile_prefix = B.wp13;
+    p.krange = B.wk13;
+    p.n_groups = (E + Ks) * P;
+    p.n_wtiles = cdiv(H, 256);
+    p.out[0] = gr->dw1;
+    p.out[1] = swiglu ? gr->dw3 : gr->dw1;
+    p.out[2] = Ks ? gr->dsw1 : gr->dw1;
+    p.out[3] = (Ks && swiglu) ? gr->dsw3 : gr->dw1;
+    p.out_ld = H;
+    p.out_cols = H;
+    p.f32_tma = 1;
+    for (int o = 0; o < 4; ++o) {
+      const bool sh = o >= 2 && Ks;  // out[2], out[3] are the shared stacks when Ks > 0
+      MOE_TRY(make_out_map_f32(&p.omap32[o], p.out[o],
+                               static_cast<uint64_t>(sh ? Ks : E) * I, H));
+    }
+    MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
+  }
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_backward(const moe_shape* s, const moe_weights* weights,
+                                      const void* u, const void* dh, void* du,
+                                      const moe_weight_grads* grads, const void* saved,
+                                      size_t saved_bytes, void* ws, size_t ws_bytes,
+                                      moe_stream_t stream) {
+  return layer_backward(s, weights, u, dh, du, grads, saved, saved_bytes, ws, ws_bytes,
+                        cs(stream));
+}
