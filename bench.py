@@ -7,9 +7,15 @@ inputs are already resident in HBM.  Prints ONE JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
 
+The headline workload is the DeepSeek-V3-shaped prefill layer (the largest
+layer that fits one GPU); the same run also times the decode-shaped layer and
+the DeepSeekMoE-16B-shaped layer (with its backward) and reports them under
+"workloads", each with its own roofline and clock record.
+
 Under torchrun every rank runs an independent replica of the layer on its own
 GPU (tokens are independent, so the layer shards by batch with no exchange);
-value = all tokens processed / the slowest rank's time.
+value = all tokens processed / the slowest rank's time.  ``--gpus N`` without
+torchrun relaunches the script under torchrun with N processes.
 """
 from __future__ import annotations
 
@@ -30,10 +36,17 @@ sys.path.insert(0, ROOT)
 from fine_grained_shared_gemm_b300 import moe as M          # noqa: E402
 from fine_grained_shared_gemm_b300 import workloads as W    # noqa: E402
 
-DEFAULT_WORKLOAD = "dsmoe16b_bf16"
+DEFAULT_WORKLOAD = "v3_prefill_bf16"
+# timed in the same run as the headline, after it
+EXTRA_WORKLOADS = ("decode_bf16", "dsmoe16b_bf16")
+# the backward is timed on this layer (the V3-shaped backward needs ~80 GB of
+# gradients and scratch besides the weights)
+BACKWARD_WORKLOAD = "dsmoe16b_bf16"
 METRIC = "MoE layer tokens/s & TFLOP/s (% bf16 peak); decode weight GB/s (% HBM)"
 L2_FLUSH_BYTES = 512 << 20     # larger than the 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+PEAK_NOTE = ("hbm_gbs is a device copy rate counting read + write bytes; a kernel that "
+             "mostly reads can exceed it")
 
 
 def dist_env():
@@ -51,6 +64,13 @@ def max_over_ranks(x: float, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(tokens_per_rank: int, seconds: float, world: int, device):
+    """(tokens/s over all ranks, slowest rank's seconds): every rank processed
+    tokens_per_rank tokens; the job took as long as its slowest rank."""
+    slowest = max_over_ranks(seconds, device)
+    return tokens_per_rank * world / slowest, slowest
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -63,10 +83,15 @@ def expert_flops(s: W.MoEShape) -> int:
     return s.T * (s.top_k + s.n_shared) * s.n_mats * 2 * s.H * s.inter
 
 
+def used_experts(s: W.MoEShape, offsets: np.ndarray) -> int:
+    """Experts whose weights a step reads: routed experts with a token, and
+    every shared expert."""
+    return int((np.diff(offsets) > 0).sum()) + s.n_shared
+
+
 def touched_weight_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
     """Expert weights a step must read at least once: every expert with a token."""
-    used = int((np.diff(offsets) > 0).sum()) + s.n_shared
-    return used * s.n_mats * s.H * s.inter * 2 + s.n_routed * s.H * 2
+    return used_experts(s, offsets) * s.n_mats * s.H * s.inter * 2
 
 
 def ffn_alg_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
@@ -75,38 +100,62 @@ def ffn_alg_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
     rows, and u once per shared expert), the activation goes out and back
     in, the outputs go out."""
     e = 2 if s.dtype == "bf16" else 4
-    used = int((np.diff(offsets) > 0).sum()) + s.n_shared
     rows = s.T * (s.top_k + s.n_shared)
-    return (used * s.n_mats * s.H * s.inter + rows * s.H * 2 + rows * s.inter * 2) * e
+    return (used_experts(s, offsets) * s.n_mats * s.H * s.inter + rows * s.H * 2
+            + rows * s.inter * 2) * e
 
 
-def ffn_roofline(shape: W.MoEShape, offsets: np.ndarray, ffn_s: float, peaks: dict) -> dict:
-    """The expert FFN's roofline entry for one launch of ffn_s seconds.
+def decode_alg_bytes(s: W.MoEShape, offsets: np.ndarray) -> int:
+    """Bytes one decode-shaped layer step must move at least: the weights of
+    every expert with a token, the routing centroids, the tokens in and the
+    output out."""
+    e = 2 if s.dtype == "bf16" else 4
+    return touched_weight_bytes(s, offsets) * e // 2 + s.n_routed * s.H * e + 2 * s.T * s.H * e
 
-    Decode-shaped layers (T·k < 2E) are timed against the HBM copy bandwidth
-    with the weights of every touched expert as the algorithmic bytes.  Other
-    layers are timed against their binding roof: the larger of the two lower
-    bounds, algorithmic FLOPs at the measured tensor peak and algorithmic
-    bytes at the measured copy bandwidth (the V3-shaped layer sits just on the
-    memory side of the ridge); the other roof is reported under other_roof.
-    """
-    flops = expert_flops(shape)
-    if shape.T * shape.top_k < 2 * shape.n_routed:
-        gb = touched_weight_bytes(shape, offsets) / ffn_s / 1e9
-        return {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4)}
-    alg_bytes = ffn_alg_bytes(shape, offsets)
-    t_flops = flops / (peaks["bf16_tflops"] * 1e12)
-    t_bytes = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+
+def is_decode(s: W.MoEShape) -> bool:
+    """Decode-shaped: fewer routed rows than two per expert, so the step is
+    bound by streaming the touched experts' weights from HBM."""
+    return s.T * s.top_k < 2 * s.n_routed
+
+
+def prefill_roofline(s: W.MoEShape, offsets: np.ndarray, ffn_s: float, peaks: dict) -> dict:
+    """The expert FFN (both grouped GEMMs, one moe_expert_ffn call of ffn_s
+    seconds) against the measured dense bf16 tensor peak (burst: the call is
+    timed on its own and lasts milliseconds), with the HBM roof of its
+    algorithmic bytes under other_roof."""
+    flops = expert_flops(s)
+    alg_bytes = ffn_alg_bytes(s, offsets)
     tf = flops / ffn_s / 1e12
     gb = alg_bytes / ffn_s / 1e9
-    tensor = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
-              "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
-    memory = {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
-              "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4),
-              "algorithmic_bytes": alg_bytes}
-    roof, other = (memory, tensor) if t_bytes > t_flops else (tensor, memory)
-    return dict(roof, other_roof=other)
+    t_flops = flops / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    return {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+            "algorithmic_flop": flops,
+            "other_roof": {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4),
+                           "algorithmic_bytes": alg_bytes},
+            "ridge": "memory side" if t_bytes > t_flops else "tensor side"}
+
+
+def decode_roofline(s: W.MoEShape, offsets: np.ndarray, layer_s: float, ffn_s: float,
+                    peaks: dict) -> dict:
+    """A decode-shaped layer against HBM: its algorithmic bytes over the whole
+    layer's time (one step), with the expert FFN's weight stream over the FFN
+    call's time alongside."""
+    b = decode_alg_bytes(s, offsets)
+    gb = b / layer_s / 1e9
+    w = touched_weight_bytes(s, offsets)
+    gb_ffn = w / ffn_s / 1e9
+    r = {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": round(gb / peaks["hbm_gbs"], 4), "algorithmic_bytes": b,
+         "experts_touched": used_experts(s, offsets),
+         "ffn_only": {"achieved": round(gb_ffn, 1), "unit": "GB/s",
+                      "frac": round(gb_ffn / peaks["hbm_gbs"], 4), "weight_bytes": w}}
+    if gb > peaks["hbm_gbs"] or gb_ffn > peaks["hbm_gbs"]:
+        r["note"] = PEAK_NOTE
+    return r
 
 
 def kernel_source_hash() -> str:
@@ -381,28 +430,16 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
                 "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"}}
 
 
-def run_cuda(args):
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    shape = W.SHAPES[args.workload]
+def measure_forward(args, shape, dev, flush, world, peaks, barrier):
+    """Time the layer forward of one workload: K steps on device-resident
+    inputs (L2 flushed before each), then K steps end to end through the
+    host-buffer entry point.  Returns (entry, layer)."""
     layer = Layer(shape, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-
     for _ in range(args.warmup):
         layer.step()
     st, code = M.moe_device_status()
     if st != M.MOE_OK:
-        raise RuntimeError(f"device status {st} code {code} after warm-up")
-
+        raise RuntimeError(f"device status {st} code {code} after warm-up ({shape.name})")
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -418,9 +455,7 @@ def run_cuda(args):
         barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ffn_ms = [a.elapsed_time(b) for a, b in ffn_ev]
-    total_s = max_over_ranks(sum(step_ms) / 1e3, dev)
-    tokens = shape.T * K * world
-    value = tokens / total_s
+    value, total_s = whole_job_rate(shape.T * K, sum(step_ms) / 1e3, world, dev)
 
     # end to end through the host-buffer entry point: H2D of u, layer, D2H of h
     u_host = layer.inp.u.cpu().pin_memory()
@@ -435,43 +470,98 @@ def run_cuda(args):
         M.moe_layer_forward_host(shape, layer.wt, u_host, h_host, u_dev, layer.h, layer.ws_l)
     e1.record()
     barrier()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+    e2e_value, _ = whole_job_rate(shape.T * K, e0.elapsed_time(e1) / 1e3, world, dev)
     st, code = M.moe_device_status()
     if st != M.MOE_OK:
-        raise RuntimeError(f"device status {st} code {code}")
+        raise RuntimeError(f"device status {st} code {code} ({shape.name})")
 
-    peaks, peak_src = load_peaks()
-    ffn_avg_s = sum(ffn_ms) / len(ffn_ms) / 1e3
-    flops = expert_flops(shape)
+    ffn_s = sum(ffn_ms) / len(ffn_ms) / 1e3
+    layer_s = sum(step_ms) / len(step_ms) / 1e3
     offsets = layer.off.cpu().numpy()
-    roof = ffn_roofline(shape, offsets, ffn_avg_s, peaks)
-    roof.update({"traffic": recorded_traffic(args.workload), "kernel": "moe_expert_ffn",
-                 "peak_source": f"{peak_src} (burst)", "ms_per_launch": round(ffn_avg_s * 1e3, 4)})
-
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if shape.dtype == "bf16" else "f32", "data": "synthetic (seeded N(0,1) tokens, "
-        "N(0,1/fan_in) weights)",
+    flops = expert_flops(shape)
+    if is_decode(shape):
+        roof = decode_roofline(shape, offsets, layer_s, ffn_s, peaks)
+        roof["kernel"] = "moe_layer_forward (all 10 launches of one step)"
+    else:
+        roof = prefill_roofline(shape, offsets, ffn_s, peaks)
+        roof["kernel"] = "moe_expert_ffn (gate/up and down grouped GEMMs)"
+    roof.update({"traffic": recorded_traffic(shape.name),
+                 "peak_source": f"{peaks.get('_source', 'measured')} (burst)",
+                 "ms_per_launch": round((layer_s if is_decode(shape) else ffn_s) * 1e3, 4)})
+    entry = {
+        "value": round(value, 1), "unit": "tokens/s",
+        "ms_per_step": round(total_s / K * 1e3, 4),
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H,
                    "n_routed": shape.n_routed, "n_shared": shape.n_shared,
                    "top_k": shape.top_k, "inter": shape.inter, "gate": shape.gate,
                    "act": shape.act, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (512 MiB write)"},
-        "expert_tflops": round(flops / ffn_avg_s / 1e12, 1),
-        "layer_tflops": round(flops / (total_s / K / world) / 1e12, 1) if world == 1 else None,
+        "expert_ffn_ms": round(ffn_s * 1e3, 4),
+        "expert_tflops": round(flops / ffn_s / 1e12, 1),
+        "layer_tflops": round(flops / layer_s / 1e12, 1),
         "roofline": roof,
-        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s",
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(u_host.numel() * u_host.element_size()),
                 "d2h_bytes_per_step": int(h_host.numel() * h_host.element_size())},
         "gpu_launches": layer.launches_per_step * K,
         "clocks": clk.summary(),
     }
-    if not args.no_backward:
-        line["backward"] = measure_backward(args, shape, layer, flush, dev, peaks)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shape, layer, args.cpu_sample)
+    del u_host, h_host, u_dev
+    return entry, layer
+
+
+def run_cuda(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    peaks = dict(peaks, _source=peak_src)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+
+    names = [args.workload]
+    if not args.only:
+        names += [n for n in EXTRA_WORKLOADS if n != args.workload]
+    entries = {}
+    cpu = None
+    for n, name in enumerate(names):
+        shape = W.SHAPES[name]
+        entry, layer = measure_forward(args, shape, dev, flush, world, peaks, barrier)
+        if not args.no_backward and name == BACKWARD_WORKLOAD:
+            entry["backward"] = measure_backward(args, shape, layer, flush, dev, peaks)
+        if n == 0 and rank == 0 and world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(shape, layer, args.cpu_sample)
+        entries[name] = entry
+        del layer
+        torch.cuda.empty_cache()
+
+    head = entries[args.workload]
+    shape = W.SHAPES[args.workload]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": head["config"],
+        "expert_ffn_ms": head["expert_ffn_ms"], "expert_tflops": head["expert_tflops"],
+        "layer_tflops": head["layer_tflops"],
+        "roofline": head["roofline"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+        "peaks_note": PEAK_NOTE,
+    }
+    if "backward" in head:
+        line["backward"] = head["backward"]
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    line["workloads"] = {k: v for k, v in entries.items() if k != args.workload}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -480,23 +570,40 @@ def run_cuda(args):
 
 # ------------------------------------------------------------------ CPU oracle legs
 
+# float64 copies of all expert weights are kept only up to this size; larger
+# layers convert each expert's stored weights when the oracle asks for them
+F64_CACHE_BYTES = 8 << 30
+
+
+def f64_weight_bytes(shape) -> int:
+    return (shape.n_routed + shape.n_shared) * shape.n_mats * shape.H * shape.inter * 8
+
+
 def _oracle_setup(shape, inp):
-    """Host float64 copies of what the oracle needs (outside any timing)."""
+    """What the oracle needs, as host float64 arrays.  Returns (O, routed_fn,
+    shared_fn, centroids, offsets, bias, cached): with cached, every expert's
+    weights are converted once and kept; otherwise each call converts the
+    stored weights again (the caller decides whether that is timed)."""
     import oracle.moe_oracle as O  # the oracle is imported only for this leg
     np64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    cached = f64_weight_bytes(shape) <= F64_CACHE_BYTES
     routed = {}
-    shared = [(np64(inp.sw1[j]), None if inp.sw3 is None else np64(inp.sw3[j]),
-               np64(inp.sw2[j])) for j in range(shape.n_shared)]
+
+    def convert(w1, w3, w2, j):
+        return (np64(w1[j]), None if w3 is None else np64(w3[j]), np64(w2[j]))
 
     def routed_fn(e):
+        if not cached:
+            return convert(inp.w1, inp.w3, inp.w2, e)
         if e not in routed:
-            routed[e] = (np64(inp.w1[e]), None if inp.w3 is None else np64(inp.w3[e]),
-                         np64(inp.w2[e]))
+            routed[e] = convert(inp.w1, inp.w3, inp.w2, e)
         return routed[e]
+
+    shared = [convert(inp.sw1, inp.sw3, inp.sw2, j) for j in range(shape.n_shared)]
     cents = np64(inp.centroids)
     off = None if inp.logit_offset is None else np64(inp.logit_offset)
     bias = None if inp.select_bias is None else inp.select_bias.cpu().numpy()
-    return O, routed_fn, (lambda j: shared[j]), cents, off, bias
+    return O, routed_fn, (lambda j: shared[j]), cents, off, bias, cached
 
 
 def _oracle_tokens(O, shape, u_rows, routed_fn, shared_fn, cents, off, bias):
@@ -504,6 +611,12 @@ def _oracle_tokens(O, shape, u_rows, routed_fn, shared_fn, cents, off, bias):
     r = O.route(z, shape.gate, shape.top_k, bias)
     O.dispatch(r["idx"], shape.n_routed)
     return O.layer_forward(u_rows, r, routed_fn, shared_fn, shape.n_shared, shape.act)
+
+
+def _preconvert(O, shape, u, routed_fn, cents, off, bias):
+    z = O.router_logits(u, cents, off)
+    for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
+        routed_fn(int(e))
 
 
 def _threads():
@@ -515,21 +628,27 @@ def _threads():
         return len(os.sched_getaffinity(0))
 
 
+def _weights_note(shape, cached):
+    if cached:
+        return "expert weights converted to float64 once, outside the timing"
+    return (f"each used expert's stored bf16 weights converted to float64 inside the timing "
+            f"(float64 copies of all {shape.n_routed + shape.n_shared} experts would take "
+            f"{f64_weight_bytes(shape) / 2**30:.0f} GiB of host memory)")
+
+
 def cpu_baseline(shape, layer, n_sample, min_seconds=10.0):
     """The oracle on bounded samples of the workload's tokens, repeated until
     about ``min_seconds`` of CPU work; tokens/s over all repetitions."""
     inp = layer.inp
-    O, routed_fn, shared_fn, cents, off, bias = _oracle_setup(shape, inp)
+    O, routed_fn, shared_fn, cents, off, bias, cached = _oracle_setup(shape, inp)
     rng = np.random.default_rng(0)
     n = min(n_sample, shape.T)
     done, elapsed, reps = 0, 0.0, 0
     while elapsed < min_seconds and reps < 64:
         rows = np.sort(rng.choice(shape.T, size=n, replace=False))
         u = inp.u[torch.from_numpy(rows).to(inp.u.device)].to(torch.float64).cpu().numpy()
-        # weights of every expert these tokens use are converted before timing
-        z = O.router_logits(u, cents, off)
-        for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
-            routed_fn(int(e))
+        if cached:
+            _preconvert(O, shape, u, routed_fn, cents, off, bias)
         t0 = time.perf_counter()
         _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
         elapsed += time.perf_counter() - t0
@@ -538,7 +657,7 @@ def cpu_baseline(shape, layer, n_sample, min_seconds=10.0):
     return {"value": round(done / elapsed, 2), "unit": "tokens/s", "cores": _threads(),
             "kind": "oracle", "sample": f"{reps} x {n} random tokens of {shape.name} "
             f"(T={shape.T}): full layer (logits, route, dispatch, FFN, combine) in float64 "
-            f"NumPy, weights pre-converted to float64 outside the timing; {elapsed:.1f} s"}
+            f"NumPy; {_weights_note(shape, cached)}; {elapsed:.1f} s"}
 
 
 def run_reference(args):
@@ -548,18 +667,18 @@ def run_reference(args):
     shape = W.SHAPES[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_inputs(shape, dev, seed=0)
-    O, routed_fn, shared_fn, cents, off, bias = _oracle_setup(shape, inp)
+    O, routed_fn, shared_fn, cents, off, bias, cached = _oracle_setup(shape, inp)
     u_all = inp.u
-    n = min(args.cpu_sample, shape.T)
+    n = args.ref_sample or (256 if cached else 8)
+    n = min(n, shape.T)
     rng = np.random.default_rng(1)
     samples = []
     for _ in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(shape.T, size=n, replace=False))
         samples.append(u_all[torch.from_numpy(rows).to(u_all.device)].to(torch.float64).cpu().numpy())
-    for u in samples:       # expert weights resident in host memory before timing
-        z = O.router_logits(u, cents, off)
-        for e in np.unique(O.route(z, shape.gate, shape.top_k, bias)["idx"]):
-            routed_fn(int(e))
+    if cached:              # expert weights resident in host memory before timing
+        for u in samples:
+            _preconvert(O, shape, u, routed_fn, cents, off, bias)
     for u in samples[:args.warmup]:
         _oracle_tokens(O, shape, u, routed_fn, shared_fn, cents, off, bias)
     t0 = time.perf_counter()
@@ -574,13 +693,28 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H,
                    "n_routed": shape.n_routed, "n_shared": shape.n_shared,
-                   "top_k": shape.top_k, "inter": shape.inter},
+                   "top_k": shape.top_k, "inter": shape.inter, "gate": shape.gate,
+                   "act": shape.act},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": _threads(),
-                         "kind": "oracle", "sample": f"{n} tokens per step of {shape.name}"},
+                         "kind": "oracle",
+                         "sample": f"{n} random tokens per step of {shape.name} "
+                                   f"(T={shape.T}); {_weights_note(shape, cached)}"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def relaunch_under_torchrun(n: int):
+    """Re-execute this script as n torchrun processes on this node."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port",
+           str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    os.execv(sys.executable, cmd)
 
 
 def main():
@@ -590,13 +724,24 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.SHAPES))
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--cpu-sample", type=int, default=256,
+                    help="tokens per sample of the cpu_baseline leg")
+    ap.add_argument("--ref-sample", type=int, default=0,
+                    help="tokens per step of --impl reference (0: 256 when the float64 "
+                         "weights fit the host cache, else 8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the timed moe_layer_backward leg")
+    ap.add_argument("--only", action="store_true",
+                    help="time the chosen workload only, not the extra ones")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    _, world, _ = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        relaunch_under_torchrun(args.gpus)
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} does not match WORLD_SIZE={world}")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -1024,19 +1024,47 @@ namespace {
 constexpr size_t kStaticDispatchEntries = 131072;  // ceil(T / 256) * n_routed
 static __device__ __align__(256) int32_t g_static_dispatch_scratch[2 * kStaticDispatchEntries];
 
-// Device address of the array on the current device, looked up once per
-// device.  Host code cannot use the symbol itself as a device pointer.
+// Device address of the array in the current context, looked up once per
+// device and context.  Host code cannot use the symbol itself as a device
+// pointer.  The lookup is repeated when the device's current context is not
+// the one the cached address was taken in (after cudaDeviceReset, or a
+// primary context released and created again, the module can be loaded at
+// another address).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 moe_status static_dispatch_scratch(void** out) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static CUcontext ctx_of[64] = {nullptr};
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return cuda_fail(cudaErrorNotSupported);
+  CUcontext ctx = nullptr;  // stays null while no context is current yet
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorNotSupported);
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (ctx == nullptr || addr[dev] == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
+    // the runtime makes the device's primary context current here if needed
     MOE_CUDA(cudaGetSymbolAddress(&p, g_static_dispatch_scratch));
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cuda_fail(cudaErrorNotSupported);
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return MOE_OK;

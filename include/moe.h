@@ -329,7 +329,9 @@ MOE_API moe_status moe_layer_forward_train(const moe_shape* shape,
  * Larger shapes return MOE_ERR_UNSUPPORTED and launch nothing.  The library
  * looks up the array's device address on the first call made on each device
  * (with that device current), so make that first call before any stream
- * capture.  All calls share the one array, and every call overwrites what it
+ * capture; it looks the address up again when the device's current context
+ * has changed since (after cudaDeviceReset, the module may be loaded at
+ * another address).  All calls share the one array, and every call overwrites what it
  * uses before reading it: calls that may overlap on the GPU (different
  * streams, or concurrent host threads) race and must be serialised by the
  * caller.  Allocates nothing. */

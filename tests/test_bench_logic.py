@@ -24,22 +24,40 @@ def test_algorithmic_work_by_hand():
     assert bench.ffn_alg_bytes(s, off) == want
 
 
-@pytest.mark.parametrize("name,bound", [("dsmoe16b_bf16", "tensor"),
-                                        ("v3_prefill_bf16", "hbm"),
-                                        ("sweep_m1", "tensor"),
-                                        ("decode_bf16", "hbm")])
-def test_binding_roof(name, bound):
+@pytest.mark.parametrize("name", ["dsmoe16b_bf16", "v3_prefill_bf16", "sweep_m1"])
+def test_prefill_roofline_is_the_tensor_peak(name):
     s = W.SHAPES[name]
-    r = bench.ffn_roofline(s, _even_offsets(s), 1e-3, PEAKS)
-    assert r["bound"] == bound
-    assert 0 < r["frac"] and r["achieved"] > 0
-    if name != "decode_bf16":
-        other = r["other_roof"]
-        assert other["bound"] != bound
-        # the binding roof is the one whose lower bound on the time is larger
-        t = {"tensor": bench.expert_flops(s) / (PEAKS["bf16_tflops"] * 1e12),
-             "hbm": bench.ffn_alg_bytes(s, _even_offsets(s)) / (PEAKS["hbm_gbs"] * 1e9)}
-        assert t[bound] >= t[other["bound"]]
+    off = _even_offsets(s)
+    r = bench.prefill_roofline(s, off, 1e-3, PEAKS)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(bench.expert_flops(s) / 1e-3 / 1e12, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["bf16_tflops"], rel=1e-3)
+    other = r["other_roof"]
+    assert other["bound"] == "hbm"
+    assert other["algorithmic_bytes"] == bench.ffn_alg_bytes(s, off)
+    # the V3-shaped layer sits just on the memory side of the ridge
+    t_f = bench.expert_flops(s) / (PEAKS["bf16_tflops"] * 1e12)
+    t_b = bench.ffn_alg_bytes(s, off) / (PEAKS["hbm_gbs"] * 1e9)
+    assert r["ridge"] == ("memory side" if t_b > t_f else "tensor side")
+
+
+def test_decode_roofline_counts_bytes_over_the_layer_time():
+    s = W.SHAPES["decode_bf16"]
+    assert bench.is_decode(s) and not bench.is_decode(W.SHAPES["v3_prefill_bf16"])
+    off = np.zeros(s.n_routed + 1, dtype=np.int64)
+    off[1:] = np.cumsum(np.r_[np.full(100, 5), np.zeros(s.n_routed - 100, dtype=np.int64)])
+    # 100 routed experts with a token + 1 shared, 3 matrices of H x I bf16
+    w = 101 * 3 * s.H * s.inter * 2
+    assert bench.touched_weight_bytes(s, off) == w
+    b = w + s.n_routed * s.H * 2 + 2 * s.T * s.H * 2
+    assert bench.decode_alg_bytes(s, off) == b
+    r = bench.decode_roofline(s, off, 2e-3, 1.8e-3, PEAKS)
+    assert r["bound"] == "hbm" and r["experts_touched"] == 101
+    assert r["achieved"] == pytest.approx(b / 2e-3 / 1e9, rel=1e-3)
+    assert r["ffn_only"]["achieved"] == pytest.approx(w / 1.8e-3 / 1e9, rel=1e-3)
+    assert "note" not in r
+    fast = bench.decode_roofline(s, off, 1e-4, 1e-4, PEAKS)   # above the copy rate
+    assert fast["frac"] > 1 and "note" in fast
 
 
 def test_backward_launch_counts():

@@ -62,3 +62,24 @@ def test_two_rank_replicas_gloo():
     slowest, err = q.get(timeout=60)
     assert slowest == 2.5
     assert err < 1e-12   # float64 BLAS may block a shard differently from the batch
+
+
+def _rate_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took 2 + r seconds for its 1000 tokens
+        value, slowest = bench.whole_job_rate(1000, 2.0 + rank, world, torch.device("cpu"))
+        out.put((rank, value, slowest))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_whole_job_rate_counts_every_rank_over_the_slowest():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    mp.spawn(_rate_worker, args=(2, _free_port(), q), nprocs=2, join=True)
+    got = sorted(q.get(timeout=60) for _ in range(2))
+    for rank, value, slowest in got:
+        assert slowest == 3.0                 # the slowest rank's time on every rank
+        assert value == 2000 / 3.0            # both ranks' tokens over that time

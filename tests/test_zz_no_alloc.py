@@ -58,8 +58,19 @@ def test_static_scratch_dispatch_matches_workspace_dispatch():
 
 @pytest.mark.gpu
 def test_static_scratch_dispatch_refuses_oversize_shapes():
-    # ceil(T / 256) * n_routed above the array's 131072 entries
-    big = M.moe_shape(T=256 * 129, H=256, n_routed=1024, n_shared=0, top_k=8, inter=128,
-                      gate=0, act=1, dtype=1)
-    st = M.lib().moe_dispatch_static(ctypes.byref(big), 256, 256, 256, 256, 256, 256, None)
+    # ceil(T / 256) * n_routed above the array's 131072 entries.  Every buffer
+    # is real and large enough for the shape, so that if the size check ever
+    # ran after the launches the call would still stay inside its buffers and
+    # this test would fail on the status, not fault the GPU.
+    shape = W.MoEShape("noalloc_big", T=256 * 129, H=256, n_routed=1024, n_shared=0,
+                       top_k=8, inter=128)
+    idx = torch.zeros((shape.T, shape.top_k), dtype=torch.int32, device=DEV)
+    idx += torch.arange(shape.top_k, dtype=torch.int32, device=DEV)
+    u = torch.zeros((shape.T, shape.H), dtype=torch.bfloat16, device=DEV)
+    out = _outputs(shape, DEV)
+    st = M.lib().moe_dispatch_static(ctypes.byref(M.shape_struct(shape)), M._ptr(idx),
+                                     M._ptr(u), *[M._ptr(t) for t in out], None)
+    torch.cuda.synchronize()
     assert st == M.MOE_ERR_UNSUPPORTED
+    assert M.moe_device_status() == (M.MOE_OK, 0)
+    assert bool((out[0] == -1).all())      # nothing was launched
