@@ -510,6 +510,100 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
     return entry, layer
 
 
+def memory_kernel_bytes(s: W.MoEShape) -> dict:
+    """Minimal DRAM bytes of each memory-bound launch of one layer step (the
+    inputs read once, the outputs written once; bf16 or fp32 rows)."""
+    e = 2 if s.dtype == "bf16" else 4
+    T, H, E, k, Ks = s.T, s.H, s.n_routed, s.top_k, s.n_shared
+    n_chunks = -(-T // 256)
+    return {
+        # logits in, bias in; choice and gate weights out
+        "route_kernel": T * E * 4 + E * 4 + T * k * 8,
+        # choice in, per-chunk histograms out
+        "dispatch_count": T * k * 4 + n_chunks * E * 4,
+        # histograms in, chunk bases and offsets out
+        "dispatch_scan": 2 * n_chunks * E * 4 + (E + 1) * 4,
+        # choice and chunk bases in, row_token and slot_row out
+        "dispatch_scatter": T * k * 4 + n_chunks * E * 4 + 2 * T * k * 4,
+        # every token row read once (from HBM; its k copies from L2), T·k rows out
+        "gather_rows": T * H * e + T * k * H * e + T * k * 4,
+        # routed outputs, shared outputs and u in, h out; slot rows and weights in
+        "combine_kernel": (T * k + T * Ks + T) * H * e + T * H * e + T * k * 8,
+    }
+
+
+def run_memory_kernels(args):
+    """Times the memory-bound kernels of one layer step (route, dispatch's
+    three kernels and row gather, combine) on a workload's token batch,
+    without allocating expert weights: the expert outputs combine reads are
+    seeded random rows.  L2 is flushed before every timed launch."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = W.SHAPES[args.workload]
+    peaks, peak_src = load_peaks()
+    inp = W.make_token_inputs(s, dev, seed=0)
+    T, H, E, k, Ks = s.T, s.H, s.n_routed, s.top_k, s.n_shared
+    dt = s.torch_dtype
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    off = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    row_token = torch.empty((T * k,), dtype=torch.int32, device=dev)
+    slot_row = torch.empty((T * k,), dtype=torch.int32, device=dev)
+    u_perm = torch.empty((T * k, H), dtype=dt, device=dev)
+    y_perm = torch.randn((T * k, H), generator=gen, device=dev).to(dt)
+    y_shared = torch.randn((Ks, T, H), generator=gen, device=dev).to(dt)
+    h = torch.empty((T, H), dtype=dt, device=dev)
+    ws = M.alloc_workspace(M.moe_dispatch_workspace_size(s), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    steps = {
+        "router_logits": lambda: M.moe_router_logits(s, inp["u"], inp["centroids"],
+                                                     inp["logit_offset"], logits),
+        "route": lambda: M.moe_route(s, logits, inp["select_bias"], idx, w),
+        "dispatch": lambda: M.moe_dispatch(s, idx, inp["u"], off, row_token, slot_row, u_perm,
+                                           ws),
+        "combine": lambda: M.moe_combine(s, inp["u"], y_perm, y_shared, w, slot_row, h),
+    }
+    for _ in range(args.warmup):
+        for f in steps.values():
+            f()
+    torch.cuda.synchronize()
+    ms = {n: [] for n in steps}
+    for _ in range(args.steps):
+        for n, f in steps.items():
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            ms[n].append((a, b))
+    torch.cuda.synchronize()
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code}")
+    alg = memory_kernel_bytes(s)
+    call_bytes = {"route": alg["route_kernel"],
+                  "dispatch": sum(alg[n] for n in ("dispatch_count", "dispatch_scan",
+                                                   "dispatch_scatter", "gather_rows")),
+                  "combine": alg["combine_kernel"],
+                  "router_logits": T * H * (2 if s.dtype == "bf16" else 4)
+                  + E * H * (2 if s.dtype == "bf16" else 4) + T * E * 4}
+    out = {}
+    for n, evs in ms.items():
+        t = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        gb = call_bytes[n] / t / 1e9
+        out[n] = {"us": round(t * 1e6, 2), "algorithmic_bytes": call_bytes[n],
+                  "gbs": round(gb, 1), "frac_of_hbm": round(gb / peaks["hbm_gbs"], 4)}
+    print(json.dumps({"mode": "memory_kernels", "workload": s.name, "steps": args.steps,
+                      "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
+                      "per_kernel_bytes": alg, "calls": out,
+                      "note": "median of CUDA-event times per C-ABI call, L2 flushed before "
+                              "each; dispatch is four kernels (count, scan, scatter, gather)"}),
+          flush=True)
+
+
 def run_cuda(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -734,6 +828,9 @@ def main():
                     help="skip the timed moe_layer_backward leg")
     ap.add_argument("--only", action="store_true",
                     help="time the chosen workload only, not the extra ones")
+    ap.add_argument("--memory-kernels", action="store_true",
+                    help="time the memory-bound kernels of the chosen workload's step "
+                         "(no expert weights are allocated)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -744,6 +841,8 @@ def main():
         sys.exit(f"bench.py: --gpus {args.gpus} does not match WORLD_SIZE={world}")
     if args.impl == "reference":
         run_reference(args)
+    elif args.memory_kernels:
+        run_memory_kernels(args)
     else:
         run_cuda(args)
 

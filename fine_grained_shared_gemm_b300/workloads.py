@@ -135,6 +135,12 @@ SHAPES = {
             description="granularity m=16 expert shape (width 256, 2048 rows per "
                         "expert) with 32 experts"),
         MoEShape(
+            name="decode_e48_bf16", T=8, H=7168, n_routed=48, n_shared=1, top_k=8,
+            inter=2048, gate=GATE_SIGMOID_BIAS, act=ACT_SWIGLU, dtype="bf16",
+            bias_range=0.1, logit_offset_std=1.0,
+            description="decode-shaped layer cut to 48 routed experts and 8 tokens: "
+                        "about 1.3 routed rows per expert as in the full decode layer"),
+        MoEShape(
             name="decode_bf16", T=64, H=7168, n_routed=384, n_shared=1, top_k=8,
             inter=2048, gate=GATE_SIGMOID_BIAS, act=ACT_SWIGLU, dtype="bf16",
             bias_range=0.1, logit_offset_std=1.0,
@@ -210,6 +216,27 @@ def make_inputs(shape: MoEShape, device="cpu", seed: int = 0) -> MoEInputs:
             a2[e] = _normal(gen, (H, I), I ** -0.5, dt, device)
     return MoEInputs(shape, u, centroids, select_bias, logit_offset,
                      w1, w3, w2, sw1, sw3, sw2)
+
+
+def make_token_inputs(shape: MoEShape, device="cpu", seed: int = 0) -> dict:
+    """The routing inputs of a layer only (u, centroids, selection bias, logit
+    offsets), equal to those of :func:`make_inputs` with the same seed: they
+    are the first draws of the documented order.  For timing the kernels that
+    never read expert weights without allocating them."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    T, H, E = shape.T, shape.H, shape.n_routed
+    u = _normal(gen, (T, H), 1.0, shape.torch_dtype, device)
+    centroids = _normal(gen, (E, H), H ** -0.5, shape.torch_dtype, device)
+    select_bias = None
+    if shape.bias_range > 0:
+        r = torch.rand((E,), generator=gen, device=device, dtype=torch.float32)
+        select_bias = (r * 2.0 - 1.0) * shape.bias_range
+    logit_offset = None
+    if shape.logit_offset_std > 0:
+        logit_offset = _normal(gen, (E,), shape.logit_offset_std, torch.float32, device)
+    return dict(u=u, centroids=centroids, select_bias=select_bias, logit_offset=logit_offset)
 
 
 def random_logits(T: int, E: int, device="cpu", seed: int = 0,
