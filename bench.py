@@ -525,8 +525,8 @@ def memory_kernel_bytes(s: W.MoEShape) -> dict:
         "dispatch_scan": 2 * n_chunks * E * 4 + (E + 1) * 4,
         # choice and chunk bases in, row_token and slot_row out
         "dispatch_scatter": T * k * 4 + n_chunks * E * 4 + 2 * T * k * 4,
-        # every token row read once (from HBM; its k copies from L2), T·k rows out
-        "gather_rows": T * H * e + T * k * H * e + T * k * 4,
+        # every token row read once and written to its k rows; slot rows in
+        "scatter_token_rows": T * H * e + T * k * H * e + T * k * 4,
         # routed outputs, shared outputs and u in, h out; slot rows and weights in
         "combine_kernel": (T * k + T * Ks + T) * H * e + T * H * e + T * k * 8,
     }
@@ -586,7 +586,7 @@ def run_memory_kernels(args):
     alg = memory_kernel_bytes(s)
     call_bytes = {"route": alg["route_kernel"],
                   "dispatch": sum(alg[n] for n in ("dispatch_count", "dispatch_scan",
-                                                   "dispatch_scatter", "gather_rows")),
+                                                   "dispatch_scatter", "scatter_token_rows")),
                   "combine": alg["combine_kernel"],
                   "router_logits": T * H * (2 if s.dtype == "bf16" else 4)
                   + E * H * (2 if s.dtype == "bf16" else 4) + T * E * 4}
@@ -600,7 +600,8 @@ def run_memory_kernels(args):
                       "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
                       "per_kernel_bytes": alg, "calls": out,
                       "note": "median of CUDA-event times per C-ABI call, L2 flushed before "
-                              "each; dispatch is four kernels (count, scan, scatter, gather)"}),
+                              "each; dispatch is four kernels (count, scan, scatter, row "
+                              "scatter)"}),
           flush=True)
 
 
@@ -679,7 +680,8 @@ def _oracle_setup(shape, inp):
     weights are converted once and kept; otherwise each call converts the
     stored weights again (the caller decides whether that is timed)."""
     import oracle.moe_oracle as O  # the oracle is imported only for this leg
-    np64 = lambda t: t.detach().to(torch.float64).cpu().numpy()
+    # copied to the host in the stored type, widened there (exact for bf16)
+    np64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
     cached = f64_weight_bytes(shape) <= F64_CACHE_BYTES
     routed = {}
 
@@ -736,7 +738,9 @@ def cpu_baseline(shape, layer, n_sample, min_seconds=10.0):
     inp = layer.inp
     O, routed_fn, shared_fn, cents, off, bias, cached = _oracle_setup(shape, inp)
     rng = np.random.default_rng(0)
-    n = min(n_sample, shape.T)
+    # a layer whose float64 weights cannot stay cached converts every used
+    # expert per sample: fewer tokens keep the leg within ~10-30 s
+    n = min(n_sample if cached else max(1, n_sample // 4), shape.T)
     done, elapsed, reps = 0, 0.0, 0
     while elapsed < min_seconds and reps < 64:
         rows = np.sort(rng.choice(shape.T, size=n, replace=False))

@@ -190,9 +190,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
                         B.dispatch_ws, st));
   }
   if (Tk > 0) {
-    const int blocks = std::max(1, std::min(cdiv(Tk, 8), num_sms() * 16));
-    gather_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(dh), T, B.row_token, B.offsets + E, H, B.d_perm);
+    const int blocks = std::max(1, std::min(cdiv(T, 8), num_sms() * 16));
+    scatter_token_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(dh), T, s->top_k, B.slot_row, H, B.d_perm);
     MOE_CUDA(cudaGetLastError());
     row_gate_kernel<<<cdiv(Tk, 256), 256, 0, st>>>(B.slot_row, B.w, Tk, B.row_gate);
     MOE_CUDA(cudaGetLastError());

@@ -8,7 +8,8 @@
 //                       prefix over experts -> expert_offsets
 //   3. dispatch_scatter each chunk assigns stable ranks (warp match + popc)
 //                       and writes slot_row / row_token
-//   4. gather_rows      u_perm[r] = u[row_token[r]] with 16-byte vectors
+//   4. scatter_token_rows  u_perm[slot_row[t, s]] = u[t]: each token row is
+//                       read once and written to its k rows (16-byte vectors)
 #pragma once
 
 #include "common.cuh"
@@ -136,30 +137,33 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   }
 }
 
-// u_perm[r] = u[row_token[r]] for the rows dispatch filled (*n_rows of them);
-// one warp per row, 16-byte vectors.
+// u_perm[slot_row[t·k + s]] = u[t] for every token t and slot s (entries of
+// -1, an invalid expert, are skipped); one warp per token.  Each token row is
+// read from HBM once and written k times, instead of being read once per
+// permuted row as a gather by row_token would (which re-reads rows that the
+// stream of writes has pushed out of L2).
 template <typename T>
-__global__ void __launch_bounds__(256) gather_rows(const T* __restrict__ u, int T_tokens,
-                                                   const int32_t* __restrict__ row_token,
-                                                   const int32_t* __restrict__ n_rows, int H,
-                                                   T* __restrict__ u_perm) {
-  constexpr int V = Vec16<T>::N;
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(256) scatter_token_rows(const T* __restrict__ u, int T_tokens,
+                                                          int k,
+                                                          const int32_t* __restrict__ slot_row,
+                                                          int H, T* __restrict__ u_perm) {
+  constexpr int kMaxK = 32;
+  __shared__ int s_row[8][kMaxK];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int nvec = H / V;
-  const int rows = __ldg(n_rows);
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-    const int t = __ldg(row_token + r);
-    if (t < 0 || t >= T_tokens) continue;
-    const uint4* s = reinterpret_cast<const uint4*>(u + static_cast<size_t>(t) * H);
-    uint4* d = reinterpret_cast<uint4*>(u_perm + static_cast<size_t>(r) * H);
-    int v = lane;
-    for (; v + 96 < nvec; v += 128) {
-      const uint4 a = __ldg(s + v), b = __ldg(s + v + 32), c = __ldg(s + v + 64),
-                  e = __ldg(s + v + 96);
-      d[v] = a; d[v + 32] = b; d[v + 64] = c; d[v + 96] = e;
+  const int nvec = H * static_cast<int>(sizeof(T)) / 16;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T_tokens; t += warps) {
+    __syncwarp();
+    if (lane < k) s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
+    __syncwarp();
+    const uint4* src = reinterpret_cast<const uint4*>(u + static_cast<size_t>(t) * H);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 x = __ldg(src + v);
+      for (int j = 0; j < k; ++j) {
+        const int r = s_row[wib][j];
+        if (r >= 0) reinterpret_cast<uint4*>(u_perm + static_cast<size_t>(r) * H)[v] = x;
+      }
     }
-    for (; v < nvec; v += 32) d[v] = __ldg(s + v);
   }
 }
 

@@ -19,6 +19,7 @@
 #include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
+#include "expert_parallel.cuh"
 #include "route.cuh"
 #include "simt_gemm.cuh"
 #include "tc_gemm.cuh"
@@ -194,11 +195,12 @@ moe_status make_map5_gate_up(CUtensorMap* m, const void* w1, const void* w3, uin
 }
 
 // bf16 output [rows, cols] row-major for the epilogue's bulk stores: box of
-// 32 columns x 32 rows, plain row-major tile in shared memory.
-moe_status make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// 32 columns x box_rows rows, plain row-major tile in shared memory.
+moe_status make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows = 32) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t box[2] = {32, box_rows};
   return encode(m, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -300,8 +302,15 @@ struct FfnWs {
   void* act;
 };
 
-size_t act_rows(const moe_shape* s) {
-  return static_cast<size_t>(s->T) * (s->top_k + s->n_shared);
+// Rows of the routed experts' input: T·k for a layer, or the rows an
+// expert-parallel rank received (moe_expert_ffn_rows).
+size_t routed_rows_of(const moe_shape* s, long long routed_rows) {
+  return routed_rows >= 0 ? static_cast<size_t>(routed_rows)
+                          : static_cast<size_t>(s->T) * s->top_k;
+}
+
+size_t act_rows(const moe_shape* s, long long routed_rows = -1) {
+  return routed_rows_of(s, routed_rows) + static_cast<size_t>(s->T) * s->n_shared;
 }
 
 // Shared experts are planned as pieces of kSharedPiece tokens (a multiple of
@@ -324,10 +333,10 @@ size_t ffn_groups(const moe_shape* s) {
   return static_cast<size_t>(s->n_routed) + static_cast<size_t>(s->n_shared) * shared_pieces(s);
 }
 
-size_t ffn_ws_bytes(const moe_shape* s) {
+size_t ffn_ws_bytes(const moe_shape* s, long long routed_rows = -1) {
   const size_t G = ffn_groups(s);
   return 2 * align256(G * sizeof(GroupDesc)) + align256((G + 1) * 4) +
-         align256(act_rows(s) * s->inter * elt_bytes(s));
+         align256(act_rows(s, routed_rows) * s->inter * elt_bytes(s));
 }
 
 FfnWs carve_ffn(void* ws, const moe_shape* s) {
@@ -468,14 +477,14 @@ moe_status do_dispatch(const moe_shape* s, const int32_t* idx, const void* u, in
   dispatch_scatter<<<n_chunks, kDispatchWarps * 32, kDispatchWarps * E * 4, st>>>(
       idx, T, k, E, d.chunk_base, row_token, slot_row);
   MOE_CUDA(cudaGetLastError());
-  const int rows = T * k;
-  const int blocks = std::max(1, std::min(cdiv(rows, 8), num_sms() * 16));
+  const int blocks = std::max(1, std::min(cdiv(T, 8), num_sms() * 16));
   if (s->dtype == MOE_DTYPE_F32)
-    gather_rows<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(u), T, row_token,
-                                               offsets + E, s->H, static_cast<float*>(u_perm));
+    scatter_token_rows<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(u), T, k,
+                                                      slot_row, s->H,
+                                                      static_cast<float*>(u_perm));
   else
-    gather_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(u), T, row_token, offsets + E, s->H,
+    scatter_token_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(u), T, k, slot_row, s->H,
         static_cast<__nv_bfloat16*>(u_perm));
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
@@ -483,9 +492,10 @@ moe_status do_dispatch(const moe_shape* s, const int32_t* idx, const void* u, in
 
 // Token tile height for the tensor-core expert GEMMs: wide tiles when experts
 // get many rows, narrow (deeper pipeline) when they get a handful.
-int ffn_bn(const moe_shape* s) {
-  const long long avg = (static_cast<long long>(s->T) * s->top_k) / s->n_routed;
-  return (avg > 48 || (s->n_shared > 0 && s->top_k == 0 && s->T > 64)) ? 256 : 64;
+int ffn_bn(const moe_shape* s, long long routed_rows = -1) {
+  const long long rr = static_cast<long long>(routed_rows_of(s, routed_rows));
+  const long long avg = rr / s->n_routed;
+  return (avg > 48 || (s->n_shared > 0 && rr == 0 && s->T > 64)) ? 256 : 64;
 }
 
 // save_a / save_c (bf16 layers, may be null): GEMM1 also stores the
@@ -494,15 +504,18 @@ int ffn_bn(const moe_shape* s) {
 moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* u,
                          const void* u_perm, const int32_t* offsets, void* y_perm,
                          void* y_shared, void* ws, cudaStream_t st, void* save_a = nullptr,
-                         void* save_c = nullptr) {
-  const int T = s->T, E = s->n_routed, Ks = s->n_shared, k = s->top_k, H = s->H,
-            I = s->inter;
-  const int G = static_cast<int>(ffn_groups(s)), Tk = T * k;
-  const int rows_act = static_cast<int>(act_rows(s));
-  if (T == 0 || rows_act == 0) return MOE_OK;
-  FfnWs f = carve_ffn(ws, s);
+                         void* save_c = nullptr, long long routed_rows = -1) {
+  const int T = s->T, E = s->n_routed, Ks = s->n_shared, H = s->H, I = s->inter;
+  const int G = static_cast<int>(ffn_groups(s));
+  const int Tk = static_cast<int>(routed_rows_of(s, routed_rows));  // routed input rows
+  const int rows_act = static_cast<int>(act_rows(s, routed_rows));
+  if (rows_act == 0) return MOE_OK;
+  // the largest group: a routed expert takes at most one row per token of a
+  // layer, or any number of the rows a rank received
+  const int max_group = std::max(T, routed_rows >= 0 ? Tk : 0);
+  FfnWs f = carve_ffn(ws, s);  // act is carved last, so the row count does not move it
   const bool f32 = s->dtype == MOE_DTYPE_F32;
-  const int bn = f32 ? kSimtTile : ffn_bn(s);
+  const int bn = f32 ? kSimtTile : ffn_bn(s, routed_rows);
   // weights read by about two token tiles or fewer stream from HBM: mix
   // heavily and lightly loaded experts through the launch
   const int by_load = (!f32 && static_cast<long long>(Tk) <= 2LL * bn * E) ? 1 : 0;
@@ -525,7 +538,7 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
     p.K = H;
     p.n_cols = I;
     p.out_ld = I;
-    dim3 g1(cdiv(I, kSimtTile), cdiv(T, kSimtTile), G);
+    dim3 g1(cdiv(I, kSimtTile), cdiv(max_group, kSimtTile), G);
     if (swiglu) simt_gemm_kernel<SIMT_SWIGLU><<<g1, 256, 0, st>>>(p);
     else simt_gemm_kernel<SIMT_RELU><<<g1, 256, 0, st>>>(p);
     MOE_CUDA(cudaGetLastError());
@@ -539,7 +552,7 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
     q.K = I;
     q.n_cols = H;
     q.out_ld = H;
-    dim3 g2(cdiv(H, kSimtTile), cdiv(T, kSimtTile), G);
+    dim3 g2(cdiv(H, kSimtTile), cdiv(max_group, kSimtTile), G);
     simt_gemm_kernel<SIMT_PLAIN><<<g2, 256, 0, st>>>(q);
     MOE_CUDA(cudaGetLastError());
     return MOE_OK;
@@ -577,6 +590,8 @@ moe_status do_expert_ffn(const moe_shape* s, const moe_weights* wt, const void* 
   p.out[0] = p.out[1] = f.act;
   MOE_TRY(make_out_map(&p.omap[0], f.act, rows_act, I));
   p.omap[1] = p.omap[0];
+  MOE_TRY(make_out_map(&p.omap16[0], f.act, rows_act, I, 16));
+  p.omap16[1] = p.omap16[0];
   p.out_ld = I;
   p.out_cols = I;
   if (save_a != nullptr) {
@@ -918,6 +933,62 @@ MOE_API moe_status moe_balance_stats(const moe_shape* s, const float* logits,
 }
 
 #include "backward_api.cuh"  // the backward's host code, in place
+
+MOE_API size_t moe_expert_ffn_rows_workspace_size(const moe_shape* s, int64_t max_rows) {
+  if (check_shape(s) != MOE_OK || max_rows < 0 || max_rows > INT_MAX / 2) return 0;
+  return ffn_ws_bytes(s, max_rows);
+}
+
+MOE_API moe_status moe_expert_ffn_rows(const moe_shape* s, const moe_weights* weights,
+                                       int64_t n_rows, const void* u, const void* x_rows,
+                                       const int32_t* expert_offsets, void* y_rows,
+                                       void* y_shared, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (n_rows < 0 || n_rows > INT_MAX / 2 ||
+      static_cast<long long>(n_rows) + static_cast<long long>(s->T) * s->n_shared > INT_MAX / 2)
+    return MOE_ERR_UNSUPPORTED;
+  if (weights == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool sw = s->act == MOE_ACT_SWIGLU;
+  if (!ok_ptr(weights->w1) || !ok_ptr(weights->w2) || (sw && !ok_ptr(weights->w3)))
+    return MOE_ERR_INVALID_ARG;
+  if (s->n_shared > 0 && s->T > 0 &&
+      (!ok_ptr(weights->sw1) || !ok_ptr(weights->sw2) || (sw && !ok_ptr(weights->sw3))))
+    return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(expert_offsets)) return MOE_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!ok_ptr(x_rows) || !ok_ptr(y_rows))) return MOE_ERR_INVALID_ARG;
+  if (s->n_shared > 0 && s->T > 0 && (!ok_ptr(u) || !ok_ptr(y_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || !al16(ws) || ws_bytes < ffn_ws_bytes(s, n_rows)) return MOE_ERR_WORKSPACE;
+  return do_expert_ffn(s, weights, u, x_rows, expert_offsets, y_rows, y_shared, ws, cs(stream),
+                       nullptr, nullptr, n_rows);
+}
+
+MOE_API moe_status moe_ep_regroup(const moe_shape* s, int32_t n_ranks, const int32_t* counts,
+                                  int64_t n_rows, const void* src, void* dst,
+                                  int32_t* expert_offsets, int32_t to_expert_major,
+                                  moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (n_ranks < 1 || static_cast<long long>(n_ranks) * s->n_routed > kRegroupThreads)
+    return MOE_ERR_UNSUPPORTED;
+  if (n_rows < 0 || n_rows > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(counts) || !ok_opt(expert_offsets)) return MOE_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!ok_ptr(src) || !ok_ptr(dst))) return MOE_ERR_INVALID_ARG;
+  const int blocks = std::max(1, std::min(cdiv(static_cast<int>(n_rows), kRegroupThreads / 32),
+                                          2 * num_sms()));
+  cudaStream_t st = cs(stream);
+  const int tem = to_expert_major != 0;
+  if (s->dtype == MOE_DTYPE_F32)
+    ep_regroup_kernel<float><<<blocks, kRegroupThreads, 0, st>>>(
+        counts, n_ranks, s->n_routed, s->H, static_cast<const float*>(src),
+        static_cast<float*>(dst), expert_offsets, tem);
+  else
+    ep_regroup_kernel<__nv_bfloat16><<<blocks, kRegroupThreads, 0, st>>>(
+        counts, n_ranks, s->n_routed, s->H, static_cast<const __nv_bfloat16*>(src),
+        static_cast<__nv_bfloat16*>(dst), expert_offsets, tem);
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
 
 MOE_API moe_status moe_layer_forward(const moe_shape* s, const moe_weights* weights,
                                      const void* u, void* h, const moe_route_outputs* route_out,

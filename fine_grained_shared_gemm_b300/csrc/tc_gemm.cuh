@@ -33,9 +33,8 @@
 //               logits, weight gradients) go straight from registers, one
 //               128-byte row segment per warp store
 //
-// The producer hands the MMA thread each stage's instruction descriptor
-// through shared memory, so the MMA thread never decodes tiles; the per-group
-// tile prefix is staged in shared memory for the decoders.
+// Every role decodes the same tile sequence from the per-group tile prefix,
+// which is staged in shared memory.
 //
 // A pipeline stage holds two k-blocks (K = 128) and is filled by exactly two
 // TMA copies: one for the weight tile and one for the token tile.  Each SM
@@ -72,7 +71,11 @@ constexpr int kUmmaK = 16;         // K of one tcgen05.mma for 16-bit inputs
 constexpr int kNumThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
-constexpr int kStageBufFloats = 4 * 32 * 33;
+// Epilogue scratch per epilogue warp: two 2 KB staging tiles for bulk
+// stores (32 x 32 bf16, or one 32 x 32 fp32 tile over both) and the SwiGLU
+// hand-off area (16 x 33 floats).
+constexpr int kEpiWarpBytes = 6272;
+constexpr int kHandoffOffset = 4096;
 constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 family
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
@@ -112,6 +115,7 @@ struct Params {
   const float* col_offset;       // EPI_F32: per-column addend, may be null
   int up_first[2];               // SwiGLU, per stack: the 5-D map lands the up rows first
   CUtensorMap omap[2];           // bf16 outputs out[0], out[1]: 2-D, box 32 columns x 32 rows
+  CUtensorMap omap16[2];         // the same outputs, box 32 columns x 16 rows (SwiGLU)
   // EPI_F32 with f32_tma: fp32 outputs out[0..3] as 2-D maps, box 32 x 32;
   // full 32-row chunks leave as bulk tensor stores
   int f32_tma;
@@ -133,7 +137,7 @@ struct Config {
   static constexpr int kStageBytes = kKPS * (kABytes + kBBytes);
   static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
   static constexpr int kPrefixBytes = ((kMaxGroups + 4) * 4 + 127) / 128 * 128;
-  static constexpr int kEpiBytes = kStageBufFloats * 4;
+  static constexpr int kEpiBytes = 4 * kEpiWarpBytes;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -490,6 +494,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "memory");
 }
 
+// tanh by the hardware approximation (one MUFU operation).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// SiLU(x) = x · sigmoid(x), with sigmoid(x) = (1 + tanh(x / 2)) / 2:
+// h + h · tanh(h) for h = x / 2.
+__device__ __forceinline__ float silu_tanh(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(h), h);
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -607,10 +625,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t done_bar = bar0 + 288u;
   uint8_t* bar_area = smem + S * C::kStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 296);
-  volatile uint32_t* idesc_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 320);
-  volatile uint32_t* boff_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 384);
   int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
-  float* stage_buf = reinterpret_cast<float*>(bar_area + C::kBarBytes + C::kPrefixBytes);
+  uint8_t* epi_area = bar_area + C::kBarBytes + C::kPrefixBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR == 2 ? cluster_rank() : 0u;
@@ -659,12 +675,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const uint64_t pol_once = l2_policy_evict_first(), pol_keep = l2_policy_evict_last();
       for (int t = first; t < total && ok; t += stride) {
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
+        const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
         const int b_land = 16 << tl.b_box;  // token rows each CTA's copy lands per k-block
         // bytes both CTAs' copies deliver to the leader's barrier per stage
         const uint32_t bytes =
             static_cast<uint32_t>(PAIR * kKPS) * (kABytes + static_cast<uint32_t>(b_land) * (kBK * 2));
-        const uint32_t idesc =
-            idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma), p.a_mn != 0 ? 1u : 0u);
         // MN-major weights: the expert, its first k row and this CTA's first
         // 64-column block
         const int a_e = p.a_mn ? tl.a_base / p.a_mn_per_expert : 0;
@@ -680,15 +695,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t sa = base + stage * C::kStageBytes;
           uint32_t fb = full_bar(stage);
           if (rank == 0) {
-            idesc_slot[stage] = idesc;
-            boff_slot[stage] = static_cast<uint32_t>(b_land) * (kBK * 2);
             mbar_arrive_expect_tx(fb, bytes);
             armed |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           }
           if (PAIR == 2) fb = map_to_rank(fb, 0);
           // weights: both k-blocks in one copy (chunk kb and kb + 1)
-          const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
           if (EPI == EPI_SWIGLU) {
             tma_load_5d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, 0, 0, tl.a_row / (kBM / 2), tl.ka0 + kb,
                               pol_a);
@@ -719,28 +731,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // TMEM holds two accumulator slots of BN columns, taken in turn, so the
+    // epilogue of one tile overlaps the next tile's MMAs.
     if (lane == 0 && rank == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, a0 = 0;
+      uint32_t phase = 0, acc_ph[2] = {0u, 0u};
       bool ok = true;
       for (int t = first; t < total && ok; t += stride) {
-        if (!mbar_wait<PAIR == 2>(tempty_bar(acc), acc_phase ^ 1)) {
+        const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, 0);
+        if (!mbar_wait<PAIR == 2>(tempty_bar(a0), acc_ph[a0] ^ 1)) {
           raise_device_error(DEV_ERR_TIMEOUT_MMA);
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int nk = p.krange != nullptr ? __ldg(p.krange + group_of(p, s_prefix, t)).z
-                                           : p.num_k_blocks;
-        for (int kb = 0; kb < nk; kb += kKPS) {
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a0 * BN);
+        const uint32_t idesc =
+            idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma), p.a_mn != 0 ? 1u : 0u);
+        const uint32_t boff = static_cast<uint32_t>(16 << tl.b_box) * (kBK * 2);
+        for (int kb = 0; kb < tl.nk; kb += kKPS) {
           if (!mbar_wait(full_bar(stage), phase)) {
             raise_device_error(DEV_ERR_TIMEOUT_MMA);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t idesc = idesc_slot[stage];
-          const uint32_t boff = boff_slot[stage];
           const uint32_t sa = base + stage * C::kStageBytes;
           // a chunk past the end of K was zero-filled: its MMAs add nothing
 #pragma unroll
@@ -761,9 +775,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit_all<PAIR>(tfull_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        tc_commit_all<PAIR>(tfull_bar(a0));
+        acc_ph[a0] ^= 1u;
+        a0 ^= 1;
       }
       // All MMAs issued by this thread complete before TMEM is freed.
       tc_commit_local<PAIR>(done_bar);
@@ -773,16 +787,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quarter this warp may read
-    float* buf = stage_buf + q * 32 * 33;
+    float* buf = reinterpret_cast<float*>(epi_area + q * kEpiWarpBytes);
+    // SwiGLU hand-off: this warp's area and its partner's
+    float* hand = reinterpret_cast<float*>(epi_area + q * kEpiWarpBytes + kHandoffOffset);
+    const float* other_hand =
+        reinterpret_cast<const float*>(epi_area + (q ^ 2) * kEpiWarpBytes + kHandoffOffset);
     // the leader's accumulator-free barriers, as shared::cluster addresses
     const uint32_t tempty_leader0 = PAIR == 2 ? map_to_rank(tempty_bar(0), 0) : tempty_bar(0);
     const uint32_t tempty_leader1 = PAIR == 2 ? map_to_rank(tempty_bar(1), 0) : tempty_bar(1);
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    int a0 = 0;
+    uint32_t acc_ph[2] = {0u, 0u};
     uint32_t n_stores = 0;  // bulk stores this warp has issued (selects the staging buffer)
+    // this warp has read accumulator slot a: tell the leader's MMA issuer
+    auto release = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR == 2) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+        else mbar_arrive(tempty_bar(a));
+      }
+      acc_ph[a] ^= 1u;
+    };
     for (int t = first; t < total; t += stride) {
       const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
-      const bool ready = mbar_wait(tfull_bar(acc), acc_phase);
+      const bool ready = mbar_wait(tfull_bar(a0), acc_ph[a0]);
       // all four epilogue warps leave together, so no named barrier is left half-arrived
       if (!named_bar_and(1, 128, ready)) {
         if (!ready) raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
@@ -790,11 +818,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       tc_fence_after();
       const bool cols_ok = tl.out_col < p.out_cols;  // a CTA half past the last row stores nothing
-      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) +
-                            (static_cast<uint32_t>(q * 32) << 16);
-      for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+      const uint32_t tlane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      // One chunk: the 32 accumulator columns from TMEM column `col` hold
+      // the tile's token rows c0 .. c0 + 31 (those below n_valid are stored).
+      // Every epilogue warp runs the same chunks (the SwiGLU hand-off below
+      // synchronises them).
+      auto chunk = [&](int col, int c0) {
+        if (c0 >= tl.n_valid) return;
         uint32_t v[32];
-        tmem_ld32(tacc + c0, v);
+        tmem_ld32(tlane + static_cast<uint32_t>(col), v);
         const int nrow = min(32, tl.n_valid - c0);  // token rows of this chunk
         // A full chunk of 32 tokens goes out as one bulk store from a bf16
         // tile in this warp's shared memory (two buffers, alternating; the
@@ -828,35 +860,64 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         auto emit = [&](auto value_of, int col_base) {
           emit_to(&p.omap[tl.out_sel], p.out[tl.out_sel], value_of, col_base);
         };
+        // 16 token rows [row0, row0 + 16) of the chunk: a full half leaves as
+        // one 32 x 16 bulk store, a partial one from registers
+        auto emit16 = [&](auto value_of, int row0, int col_base) {
+          if (!cols_ok) return;
+          const int mrows = min(16, nrow - row0);
+          if (mrows <= 0) return;
+          if (mrows == 16) {
+            uint16_t* stg = reinterpret_cast<uint16_t*>(buf) + (n_stores & 1) * 1024;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(value_of(j)));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.omap16[tl.out_sel], smem_u32(stg), tl.out_col + col_base,
+                           tl.out_row + c0 + row0);
+              bulk_commit();
+            }
+            ++n_stores;
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out[tl.out_sel]) +
+                               static_cast<size_t>(tl.out_row + c0 + row0) * p.out_ld +
+                               tl.out_col + col_base + lane;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < mrows) o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(value_of(j));
+          }
+        };
         if (EPI == EPI_SWIGLU) {
           // lanes 0..63 hold the gate rows and 64..127 the matching up rows
-          // (the other way round when the map lands W3 first); the warps
-          // holding up values hand them (fp32) to the partner warp q ^ 2
+          // (the other way round when the map lands W3 first): warp q and
+          // its partner q ^ 2 hold the gate and the up values of the same 32
+          // output columns.  They split the chunk's tokens: the gate warp
+          // computes tokens [0, 16) and hands the gate values of [16, 32) to
+          // the up warp, which computes [16, 32) and hands over the up values
+          // of [0, 16).  Each warp then stores its 16 rows.
           const bool gate_warp = (q < 2) != (p.up_first[tl.a_sel] != 0);
-          if (!gate_warp) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]);
-          }
+          for (int i = 0; i < 16; ++i)
+            hand[i * 33 + lane] = __uint_as_float(gate_warp ? v[16 + i] : v[i]);
           named_bar_sync(1, 128);
-          // the gate warps take the up values into registers, so that the
-          // hand-off area is free again at the second barrier and the up
-          // warps' next chunk overlaps this chunk's activation and stores
-          float upv[32];
-          if (gate_warp) {
-            const float* up = stage_buf + (q ^ 2) * 32 * 33;
+          // the partner's values into registers, so that the hand-off area
+          // is free again at the second barrier
+          float pv[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) upv[j] = up[j * 33 + lane];
-          }
+          for (int i = 0; i < 16; ++i) pv[i] = other_hand[i * 33 + lane];
           named_bar_sync(1, 128);
-          if (gate_warp) {
-            emit([&](int j) {
-              const float g = __uint_as_float(v[j]);
-              return __fdividef(g, 1.0f + __expf(-g)) * upv[j];
-            }, (q & 1) * 32);
-            if (p.save)  // the gate pre-activation too, for a later backward
-              emit_to(&p.save_map[0], p.save_out[0],
-                      [&](int j) { return __uint_as_float(v[j]); }, (q & 1) * 32);
-          } else if (p.save && cols_ok) {
+          emit16([&](int i) {
+            const float g = gate_warp ? __uint_as_float(v[i]) : pv[i];
+            const float up = gate_warp ? pv[i] : __uint_as_float(v[16 + i]);
+            return silu_tanh(g) * up;
+          }, gate_warp ? 0 : 16, (q & 1) * 32);
+          if (gate_warp && p.save)  // the gate pre-activation too, for a later backward
+            emit_to(&p.save_map[0], p.save_out[0],
+                    [&](int j) { return __uint_as_float(v[j]); }, (q & 1) * 32);
+          else if (p.save && cols_ok) {
             // the up warp stores the up pre-activation it holds (same output
             // columns as its partner's): 64 contiguous bytes per token row
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.save_out[1]) +
@@ -916,16 +977,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             emit_to(&p.save_map[0], p.save_out[0], [&](int j) { return __uint_as_float(v[j]); },
                     q * 32);
         }
-      }
-      // this warp has read the accumulator: tell the leader's MMA issuer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR == 2) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
-        else mbar_arrive(tempty_bar(acc));
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      };
+      // column c of the slot holds token row c of the tile (one call site
+      // keeps the chunk body inlined once)
+      for (int c0 = 0; c0 < tl.n_valid; c0 += 32) chunk(a0 * BN + c0, c0);
+      release(a0);
+      a0 ^= 1;
     }
     if (lane == 0) bulk_wait_all();  // every bulk store has completed before the CTA exits
     __syncwarp();

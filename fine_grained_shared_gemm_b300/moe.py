@@ -87,6 +87,11 @@ _SIGNATURES = {
     "moe_layer_forward_train": (ctypes.c_int, [_S, _W, _P, _P, _P, ctypes.c_size_t, _P,
                                                ctypes.c_size_t, _P]),
     "moe_balance_stats": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_ffn_rows_workspace_size": (ctypes.c_size_t, [_S, ctypes.c_int64]),
+    "moe_expert_ffn_rows": (ctypes.c_int, [_S, _W, ctypes.c_int64, _P, _P, _P, _P, _P, _P,
+                                           ctypes.c_size_t, _P]),
+    "moe_ep_regroup": (ctypes.c_int, [_S, ctypes.c_int32, _P, ctypes.c_int64, _P, _P, _P,
+                                      ctypes.c_int32, _P]),
 }
 
 _lib = None
@@ -293,3 +298,26 @@ def moe_layer_forward_train(shape, weights: moe_weights, u, h, saved, ws, stream
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     """A byte buffer for the ``ws`` argument (at least 256 bytes)."""
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def moe_expert_ffn_rows_workspace_size(shape, max_rows: int) -> int:
+    return lib().moe_expert_ffn_rows_workspace_size(ctypes.byref(shape_struct(shape)),
+                                                     int(max_rows))
+
+
+def moe_expert_ffn_rows(shape, weights: moe_weights, n_rows: int, u, x_rows, expert_offsets,
+                        y_rows, y_shared, ws, stream=None):
+    """Expert FFNs on explicitly given rows (an expert-parallel rank's received
+    rows): see include/moe.h."""
+    _check("moe_expert_ffn_rows", lib().moe_expert_ffn_rows(
+        ctypes.byref(shape_struct(shape)), ctypes.byref(weights), int(n_rows), _ptr(u),
+        _ptr(x_rows), _ptr(expert_offsets), _ptr(y_rows), _ptr(y_shared), _ptr(ws), _nbytes(ws),
+        _stream(stream)))
+
+
+def moe_ep_regroup(shape, n_ranks: int, counts, n_rows: int, src, dst, expert_offsets=None,
+                   to_expert_major: bool = True, stream=None):
+    """Source-major <-> expert-major order of the rows a rank received."""
+    _check("moe_ep_regroup", lib().moe_ep_regroup(
+        ctypes.byref(shape_struct(shape)), int(n_ranks), _ptr(counts), int(n_rows), _ptr(src),
+        _ptr(dst), _ptr(expert_offsets), 1 if to_expert_major else 0, _stream(stream)))

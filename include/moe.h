@@ -316,6 +316,47 @@ MOE_API moe_status moe_layer_forward_train(const moe_shape* shape,
                                            size_t saved_bytes, void* ws,
                                            size_t ws_bytes, moe_stream_t stream);
 
+/* ---- Expert parallelism (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE",
+ * llm-infra-atlas, §3.2: the routed experts are spread over devices and token
+ * rows reach them through all-to-all exchanges; the shared experts are
+ * replicated on every device and need no exchange).  With D ranks, rank d
+ * holds routed experts [d·E_loc, (d+1)·E_loc), E_loc = E / D.  A rank's
+ * moe_dispatch output is already grouped by destination (rows sorted by
+ * expert); the caller exchanges the per-expert counts and the rows (NCCL or
+ * any all-to-all), and these two calls do the local part: */
+
+/* Expert FFNs on rows given explicitly (the rows an expert-parallel rank
+ * received), same arithmetic as moe_expert_ffn.  shape: this rank's layer —
+ * T local tokens (the shared experts run on u [T, H]), n_routed = E_loc
+ * local experts, top_k ignored (0 is valid).  Routed expert e runs on rows
+ * [expert_offsets[e], expert_offsets[e+1]) of x_rows [n_rows, H] and writes
+ * the same rows of y_rows [n_rows, H]; expert_offsets [E_loc + 1] (device)
+ * must end at n_rows.  n_rows = 0 with zero offsets runs the shared experts
+ * only; shape->n_shared = 0 runs the routed experts only.  weights: w1/w3/w2
+ * hold this rank's E_loc experts ([E_loc, I, H] and [E_loc, H, I]).  ws:
+ * moe_expert_ffn_rows_workspace_size(shape, m) bytes for any n_rows <= m. */
+MOE_API size_t moe_expert_ffn_rows_workspace_size(const moe_shape* shape, int64_t max_rows);
+MOE_API moe_status moe_expert_ffn_rows(const moe_shape* shape, const moe_weights* weights,
+                                       int64_t n_rows, const void* u, const void* x_rows,
+                                       const int32_t* expert_offsets, void* y_rows,
+                                       void* y_shared, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
+
+/* Moves the n_rows rows a rank received between the order the exchange
+ * delivers (source-major: for each source rank s, for each local expert e,
+ * the rows s sent to e) and the order the expert GEMMs read (expert-major:
+ * for each local expert e, for each source s).  counts [n_ranks · E_loc]
+ * (device, int32): counts[s · E_loc + e] rows from source s for local expert
+ * e, summing to n_rows; shape->n_routed = E_loc, shape->H and ->dtype give
+ * the row size.  to_expert_major != 0: src is source-major, dst
+ * expert-major; 0: the inverse.  expert_offsets (device, may be NULL) [E_loc
+ * + 1] out: the expert-major offsets.  n_ranks · E_loc <= 1024.  src and dst
+ * [n_rows, H] may not alias.  No scratch, no host synchronisation. */
+MOE_API moe_status moe_ep_regroup(const moe_shape* shape, int32_t n_ranks,
+                                  const int32_t* counts, int64_t n_rows, const void* src,
+                                  void* dst, int32_t* expert_offsets,
+                                  int32_t to_expert_major, moe_stream_t stream);
+
 /* moe_dispatch without a workspace argument, for callers that cannot
  * allocate device memory: a runtime whose allocator already owns all of the
  * GPU's memory and has no scratch to lend, or a latency-critical path that

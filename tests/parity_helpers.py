@@ -14,7 +14,8 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}   # max|Δ| ≤ TOL · max|ref| on layer and F
 
 
 def np64(t: torch.Tensor) -> np.ndarray:
-    return t.detach().to(torch.float64).cpu().numpy()
+    """float64 copy on the host (copied in the stored type, widened there)."""
+    return t.detach().cpu().to(torch.float64).numpy()
 
 
 def expert_fns(inp: W.MoEInputs):

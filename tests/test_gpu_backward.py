@@ -161,8 +161,9 @@ def test_backward_rejects_unsupported_shapes():
 
 
 # Full-size page-shaped layers in the configuration the benchmark times:
-# (shape name, sampled tokens for du, sampled routed experts for dW).
-FULL = [("dsmoe16b_bf16", 12, 3), ("v3_prefill_bf16", 6, 3)]
+# (shape name, sampled tokens for du, sampled routed experts for dW; the most
+# loaded expert is always among them).
+FULL = [("dsmoe16b_bf16", 64, 8), ("v3_prefill_bf16", 64, 8)]
 
 
 @pytest.mark.parametrize("name,n_tok,n_exp", FULL, ids=[f[0] for f in FULL])
@@ -171,7 +172,8 @@ def test_layer_backward_full_size_sampled(name, n_tok, n_exp):
     token), the weight gradients of sampled routed experts (over all the rows
     that chose them) and of the first shared expert (over all tokens).  The
     centroid gradient sums dz over every token, which needs every expert's
-    output for every token: it is checked on the small layers only."""
+    output for every token: it is checked on the small layers and on the
+    mid-size layer below."""
     shape = W.SHAPES[name]
     inp = W.make_inputs(shape, DEV, seed=0)
     gen = torch.Generator(device=DEV)
@@ -193,7 +195,9 @@ def test_layer_backward_full_size_sampled(name, n_tok, n_exp):
     # weight gradients of sampled routed experts: every row that chose them
     gw, _ = O.gate_weights(z, idx, shape.gate)
     counts = np.bincount(idx.reshape(-1), minlength=shape.n_routed)
-    for e in rng.choice(np.nonzero(counts)[0], size=n_exp, replace=False):
+    heavy = int(np.argmax(counts))
+    others = np.setdiff1d(np.nonzero(counts)[0], [heavy])
+    for e in [heavy] + list(rng.choice(others, size=n_exp - 1, replace=False)):
         tt, ss = np.nonzero(idx == e)
         w1, w3, w2 = routed(int(e))
         _, dw1, dw3, dw2 = O.expert_ffn_backward(u[tt], w1, w2, w3, shape.act,
@@ -269,3 +273,24 @@ def test_autograd_layer_matches_oracle():
         assert grad is not None and grad.dtype == torch.bfloat16, name
         # the parameter's bf16 gradient against the oracle (one more rounding)
         assert_close(f(grad), ref[key], tol, name)
+
+
+def test_layer_backward_mid_size_every_gradient():
+    """A mid-size layer (2048 tokens, H = 2048, 64 routed experts with several
+    token tiles each, two shared experts) where the oracle can evaluate every
+    token: du, the centroid gradient (a sum of dz over all 2048 tokens) and
+    every weight gradient, element by element."""
+    shape = _shape("bwd_mid", T=2048, H=2048, n_routed=64, n_shared=2, top_k=6, inter=512)
+    inp = W.make_inputs(shape, DEV, seed=0)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    du, g = run_backward(shape, inp, dh)
+    torch.cuda.synchronize()
+    z, idx = forward_routing(shape, inp)
+    ref = oracle_backward(shape, inp, dh, z, idx)
+    tol = TOL["bf16"]
+    assert_close(np64(du), ref["du"], tol, "du")
+    assert_close(np64(g["d_centroids"]), ref["d_centroids"], tol, "d_centroids")
+    for key in ("dw1", "dw3", "dw2", "dsw1", "dsw3", "dsw2"):
+        assert_close(np64(g[key]), ref[key], tol, key)

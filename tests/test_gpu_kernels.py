@@ -296,3 +296,99 @@ def test_combine_zero_gates_is_residual():
     h = torch.empty_like(u)
     M.moe_combine(shape, u, y, None, torch.zeros((T, k), device=DEV), slot, h)
     assert torch.equal(h, u)
+
+
+# ---------------------------------------------------------------- expert FFN: tile spans
+
+def _idx_with_counts(counts, seed):
+    """A top-1 choice in which expert e receives exactly counts[e] tokens, in a
+    seeded random token order."""
+    idx = np.repeat(np.arange(len(counts)), counts)
+    np.random.default_rng(seed).shuffle(idx)
+    return idx[:, None]
+
+
+# Per-expert row counts around the token-tile boundaries of the CTA-pair
+# GEMM (256-row tiles, MMA N in steps of 32): empty, one row, one partial
+# step, a full tile, a full tile and a one-row tail, tails of every size
+# class, several full tiles with and without a tail.
+SPAN_COUNTS = [0, 1, 31, 256, 257, 300, 320, 383, 448, 511, 512, 513, 520, 748, 1024, 1025, 1100]
+
+
+@pytest.mark.parametrize("H,inter,act", [(640, 128, W.ACT_SWIGLU), (1024, 192, W.ACT_SWIGLU),
+                                         (384, 256, W.ACT_RELU)])
+def test_expert_ffn_tile_spans(H, inter, act):
+    """Every routed row and every shared row against the oracle, for expert
+    loads on both sides of each token-tile boundary; inter = 192 gives the
+    down projection an odd number of k-blocks, the shared expert's rows end in
+    a short piece."""
+    counts = np.array(SPAN_COUNTS)
+    T = int(counts.sum())
+    shape = S("ffn_spans", T=T, H=H, n_routed=len(counts), n_shared=1, top_k=1, inter=inter,
+              act=act)
+    inp = W.make_inputs(shape, DEV, seed=13)
+    idx = _idx_with_counts(counts, seed=H)
+    off, row_token, slot_row, u_perm = _gpu_dispatch(shape, idx, inp.u)
+    E = shape.n_routed
+    y_perm = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    y_shared = torch.zeros((1, T, H), dtype=torch.bfloat16, device=DEV)
+    ws = M.alloc_workspace(M.moe_expert_ffn_workspace_size(shape), DEV)
+    M.moe_expert_ffn(shape, M.weights_struct(inp), inp.u, u_perm, off, y_perm, y_shared, ws)
+    st, code = M.moe_device_status()
+    assert st == M.MOE_OK, (st, code)
+    routed, shared = expert_fns(inp)
+    u = np64(inp.u)
+    ref = O.dispatch(idx, E)
+    assert np.array_equal(np.diff(ref["offsets"]), counts)
+    yp = np64(y_perm)
+    for e in range(E):
+        r0, r1 = ref["offsets"][e], ref["offsets"][e + 1]
+        if r1 == r0:
+            continue
+        w1, w3, w2 = routed(e)
+        want = O.expert_ffn(u[ref["row_token"][r0:r1]], w1, w2, w3, act)
+        assert_close(yp[r0:r1], want, TOL["bf16"], f"expert {e} ({counts[e]} rows)")
+    w1, w3, w2 = shared(0)
+    assert_close(np64(y_shared[0]), O.expert_ffn(u, w1, w2, w3, act), TOL["bf16"], "shared")
+
+
+def test_v3_expert_ffn_whole_experts_full_size():
+    """The DeepSeek-V3-shaped layer at full size (K = 7168, 256 routed experts
+    with skewed loads from the sigmoid + bias router), moe_expert_ffn in the
+    benchmark's launch configuration: every row of the most loaded routed
+    expert (two full token tiles and a tail), of one expert with 257..511
+    rows (a full tile and a tail on the CTA pair) and of one with at most 256
+    rows (one tile), and 512 sampled rows of the shared expert."""
+    shape = W.SHAPES["v3_prefill_bf16"]
+    inp = W.make_inputs(shape, DEV, seed=0)
+    T, E, k, H = shape.T, shape.n_routed, shape.top_k, shape.H
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    M.moe_router_logits(shape, inp.u, inp.centroids, inp.logit_offset, logits)
+    idx_t, w_t, _ = gpu_route(shape, logits, inp.select_bias)
+    off, row_token, slot_row, u_perm = _gpu_dispatch(shape, idx_t.cpu().numpy(), inp.u)
+    y_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=DEV)
+    y_shared = torch.empty((1, T, H), dtype=torch.bfloat16, device=DEV)
+    ws = M.alloc_workspace(M.moe_expert_ffn_workspace_size(shape), DEV)
+    M.moe_expert_ffn(shape, M.weights_struct(inp), inp.u, u_perm, off, y_perm, y_shared, ws)
+    st, code = M.moe_device_status()
+    assert st == M.MOE_OK, (st, code)
+    offsets = off.cpu().numpy()
+    counts = np.diff(offsets)
+    heavy = int(np.argmax(counts))
+    mid = [e for e in range(E) if 257 <= counts[e] <= 511]
+    light = [e for e in range(E) if 0 < counts[e] <= 256]
+    assert counts[heavy] > 512 and mid and light, counts
+    routed, shared = expert_fns(inp)
+    rt = row_token.cpu().numpy()
+    for e in (heavy, mid[0], light[0]):
+        r0, r1 = offsets[e], offsets[e + 1]
+        x = np64(inp.u[torch.from_numpy(rt[r0:r1]).to(DEV).long()])
+        w1, w3, w2 = routed(e)
+        want = O.expert_ffn(x, w1, w2, w3, shape.act)
+        assert_close(np64(y_perm[r0:r1]), want, TOL["bf16"], f"expert {e} ({counts[e]} rows)")
+    rows = np.sort(np.random.default_rng(1).choice(T, size=512, replace=False))
+    w1, w3, w2 = shared(0)
+    want = O.expert_ffn(np64(inp.u)[rows], w1, w2, w3, shape.act)
+    assert_close(np64(y_shared[0])[rows], want, TOL["bf16"], "shared expert")
+    del inp, y_perm, y_shared, u_perm, ws
+    torch.cuda.empty_cache()

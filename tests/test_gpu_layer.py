@@ -135,10 +135,10 @@ def test_layer_host_buffers_pipelined_chunks_match_device_path():
     assert torch.equal(h_host, h_dev_path.cpu())
 
 
-# full-size page-shaped layers: (shape name, sampled tokens)
-FULL = [("dsmoe16b_bf16", 48), ("v3_prefill_bf16", 12), ("decode_bf16", 8),
-        ("v3_prefill_e32_bf16", 16), ("sweep_m16_e32_bf16", 24)] + \
-    [(f"sweep_m{m}{v}", 24) for v in ("", "_shared1") for m in (1, 2, 4, 8, 16)]
+# full-size page-shaped layers: (shape name, sampled tokens; None = every token)
+FULL = [("dsmoe16b_bf16", 512), ("v3_prefill_bf16", 512), ("decode_bf16", None),
+        ("v3_prefill_e32_bf16", 512), ("sweep_m16_e32_bf16", 512)] + \
+    [(f"sweep_m{m}{v}", 512) for v in ("", "_shared1") for m in (1, 2, 4, 8, 16)]
 
 
 @pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])
@@ -146,7 +146,8 @@ def test_layer_full_size_sampled(name, n_sample):
     shape = W.SHAPES[name]
     inp = W.make_inputs(shape, DEV, seed=0)
     h, ro = run_layer(shape, inp)
-    rows = np.sort(np.random.default_rng(0).choice(shape.T, size=n_sample, replace=False))
+    rows = None if n_sample is None else \
+        np.sort(np.random.default_rng(0).choice(shape.T, size=n_sample, replace=False))
     info = check_layer(shape, inp, h, ro, rows=rows)
     print(f"{name}: {info}")
     del inp, h, ro
