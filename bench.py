@@ -333,13 +333,12 @@ def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
     if not saved:
         n += 2 + (4 if k else 1)                  # router logits, route, dispatch
         n += (2 if sw else 1) if rows else 0      # pre-activations recomputed
-    n += 2 if k else 0                            # gather dh rows, row gate weights
+    n += 2 if k else 0                            # scatter dh rows, row gate weights
     n += 2                                        # FFN plan, weight-gradient plan
     n += 1 if rows else 0                         # dm = dh W2
     n += s.n_shared + (1 if k else 0)             # activation derivative
-    n += 1 + 3                                    # gate, router GEMMs + u transpose
+    n += 1 + 2                                    # gate, router GEMMs
     n += (1 if rows else 0) + 1                   # dx, du
-    n += 1 + (2 if k else 0)                      # dh and routed x, dh transposes
     n += 2                                        # weight-gradient GEMMs
     return n
 

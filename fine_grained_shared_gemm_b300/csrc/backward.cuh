@@ -6,15 +6,15 @@
 // selection bias only changes the choice, so neither passes a gradient.
 //
 // The tensor-core grouped GEMM does the contractions (the input-gradient
-// GEMMs read the weights MN-major, in their stored layout); the kernels here
-// produce its other operands and consume its outputs:
-//   transpose_kernel       token rows into K-major operands for the weight
-//                          gradients, which contract over each expert's own
-//                          token rows (padded per expert to kSegAlign zeros)
+// GEMMs read the weights MN-major, in their stored layout; the weight
+// gradients read the token rows x, dh and u MN-major, in theirs); the kernels
+// here produce its other operands and consume its outputs:
 //   act_backward_kernel    SwiGLU / ReLU derivative per row, written row-major
-//                          and K-major, the gate-scaled activation (K-major,
-//                          for dW2) and the per-row <dy, y> for the gate
-//                          gradient
+//                          and K-major (chunk-major, each expert's rows
+//                          padded with zeros to kSegAlign: the weight
+//                          gradients contract over each expert's own rows),
+//                          the gate-scaled activation (K-major, for dW2) and
+//                          the per-row <dy, y> for the gate gradient
 //   gate_backward_kernel   dL/dz from dL/dg through softmax or the normalised
 //                          sigmoid (dz · centroids and dzᵀ · u are grouped
 //                          GEMMs too)
@@ -35,67 +35,6 @@ namespace moe {
 // the grouped GEMM (two 64-element k-blocks).
 constexpr int kSegAlign = 128;
 
-// ---------------------------------------------------------------- transposes
-
-// dst[c][col0 + j] = src[row(j)][c] for 64 x 64 tiles through shared memory,
-// src row-major with row pitch `cols`, dst chunk-major — the layout the
-// weight-gradient GEMMs read: element (c, j) at ((j / 64) · cols + c) · 64 +
-// j % 64, so that one 64-column chunk of all `cols` rows is contiguous and a
-// TMA box of rows reads one block (col0 % 64 == 0).  Two layouts of the
-// j -> row map:
-//   seg_start == nullptr: row(j) = j; columns j >= rows_total (up to the
-//     grid's width) are written as zeros;
-//   seg_start != nullptr: the columns are per-expert segments: expert e owns
-//     [seg_start[e], seg_start[e+1]) and row(j) = offsets[e] + j - seg_start[e]
-//     while that is below offsets[e+1], zeros after; tiles at or past
-//     seg_start[E] write nothing.
-// cols % 64 == 0.
-__global__ void __launch_bounds__(256) transpose_kernel(
-    const __nv_bfloat16* __restrict__ src, int cols, int rows_total,
-    const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets, int E,
-    __nv_bfloat16* __restrict__ dst, long long col0) {
-  __shared__ uint16_t tile[64][66];
-  const int j0 = blockIdx.x * 64;   // first dst column (relative to col0)
-  const int c0 = blockIdx.y * 64;   // first feature
-  int row0, valid;                  // source row of column j0, valid columns of the tile
-  if (seg_start == nullptr) {
-    row0 = j0;
-    valid = max(0, min(64, rows_total - j0));
-  } else {
-    if (j0 >= seg_start[E]) return;
-    int lo = 0, hi = E;             // largest e with seg_start[e] <= j0
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (seg_start[mid] <= j0) lo = mid; else hi = mid;
-    }
-    const int local = j0 - seg_start[lo];
-    row0 = offsets[lo] + local;
-    valid = max(0, min(64, offsets[lo + 1] - offsets[lo] - local));
-  }
-  // load: 64 source rows x 64 features, 16 bytes per thread and step
-  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
-    const int r = i >> 3, v = i & 7;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (r < valid)
-      x = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row0 + r) * cols +
-                                               c0 + v * 8));
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(&x);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) tile[r][v * 8 + q] = h[q];
-  }
-  __syncthreads();
-  // store: 64 features x 64 columns, 16 bytes per thread and step
-  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
-    const int c = i >> 3, v = i & 7;
-    uint4 x;
-    uint16_t* h = reinterpret_cast<uint16_t*>(&x);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) h[q] = tile[v * 8 + q][c];
-    const size_t at = (static_cast<size_t>((col0 + j0) >> 6) * cols + c0 + c) * 64 + v * 8;
-    *reinterpret_cast<uint4*>(dst + at) = x;
-  }
-}
-
 // ---------------------------------------------------------------- per-row derivative
 
 // For row r of the expert inputs (routed rows [0, Tk), then shared rows) with
@@ -105,25 +44,27 @@ __global__ void __launch_bounds__(256) transpose_kernel(
 //           = g dm ⊙ [a > 0]                            (ReLU, I wide)
 //   g act   with act = SiLU(a) ⊙ c, or ReLU(a)
 //   <dm, act> (= dL/dg of the row)
-// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One block per 64 rows x 64 features:
-// dh1 is written row-major (the input-gradient GEMM's operand) and, with g
-// act, also chunk-major K-major like transpose_kernel writes (the weight
-// gradients' operands: dh1ᵀ with P·I rows, (g act)ᵀ with I rows, column
-// col0 + j for row(j)); the 64 features' share of <dm, act> goes to
-// dg_part[r · (I / 64) + blockIdx.y] (routed rows only), summed later in
-// block order.  Rows come as in transpose_kernel: a run of rows_total rows
-// from row_base (seg_start == nullptr), or the routed rows in per-expert
-// segments; columns with no row get zeros.
+// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One block per 64 rows x 64 features.
+// dh1 and g act are written row-major into the padded row space the
+// weight-gradient and input-gradient GEMMs read: each shared expert's T rows
+// padded with zero rows to Tpad, then each routed expert's rows padded with
+// zero rows to kSegAlign (dh1p [KA, P·I], gactp [KA, I]; the block's padded
+// rows start at prow0 + blockIdx.x · 64).  The block's source rows: a run of
+// rows_total rows from row_base (seg_start == nullptr; row(j) = row_base +
+// j), or the routed rows by expert segment (expert e owns padded rows
+// [seg_start[e], seg_start[e+1]) of the routed region and row(j) =
+// offsets[e] + j - seg_start[e] while that is below offsets[e+1]); padded
+// rows with no source row are written as zeros.  The 64 features' share of
+// <dm, act> goes to dg_part[r · (I / 64) + blockIdx.y] (routed rows only),
+// summed later in block order.
 template <bool SWIGLU>
 __global__ void __launch_bounds__(256) act_backward_kernel(
     const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ c,
     const __nv_bfloat16* __restrict__ dm, const float* __restrict__ row_gate, long long Tk,
     int I, long long row_base, int rows_total, const int32_t* __restrict__ seg_start,
-    const int32_t* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ dh1,
-    __nv_bfloat16* __restrict__ d1T, __nv_bfloat16* __restrict__ aT, long long col0,
-    float* __restrict__ dg_part) {
+    const int32_t* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ dh1p,
+    __nv_bfloat16* __restrict__ gactp, long long prow0, float* __restrict__ dg_part) {
   constexpr int P = SWIGLU ? 2 : 1;
-  __shared__ uint16_t t_da[64][66], t_dc[SWIGLU ? 64 : 1][66], t_ag[64][66];
   const int j0 = blockIdx.x * 64;
   const int f0 = blockIdx.y * 64;
   const int nb = I / 64;
@@ -174,43 +115,20 @@ __global__ void __launch_bounds__(256) act_backward_kernel(
           ag[q] = g * act;
         }
       }
-      const size_t off1 = static_cast<size_t>(R) * (P * I) + f0 + v * 8;
-      Vec16<__nv_bfloat16>::store(dh1 + off1, da);
-      if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1 + off1 + I, dc);
     } else {
 #pragma unroll
       for (int q = 0; q < 8; ++q) da[q] = dc[q] = ag[q] = 0.0f;
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      t_da[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(da[q]));
-      if (SWIGLU) t_dc[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(dc[q]));
-      t_ag[r][v * 8 + q] = __bfloat16_as_ushort(__float2bfloat16_rn(ag[q]));
-    }
+    const size_t prow = static_cast<size_t>(prow0 + j0 + r);
+    Vec16<__nv_bfloat16>::store(dh1p + prow * (P * I) + f0 + v * 8, da);
+    if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1p + prow * (P * I) + I + f0 + v * 8, dc);
+    Vec16<__nv_bfloat16>::store(gactp + prow * I + f0 + v * 8, ag);
     // the row's 8 vectors sit in 8 consecutive lanes: add them in a fixed order
     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
     dot += __shfl_xor_sync(0xffffffffu, dot, 4);
     if (v == 0 && r < valid && row0 + r < Tk)
       dg_part[static_cast<size_t>(row0 + r) * nb + blockIdx.y] = dot;
-  }
-  __syncthreads();
-  const size_t chunk = static_cast<size_t>((col0 + j0) >> 6);
-  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
-    const int f = i >> 3, v = i & 7;
-    uint4 xd, xc, xa;
-    uint16_t* hd = reinterpret_cast<uint16_t*>(&xd);
-    uint16_t* hc = reinterpret_cast<uint16_t*>(&xc);
-    uint16_t* ha = reinterpret_cast<uint16_t*>(&xa);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      hd[q] = t_da[v * 8 + q][f];
-      if (SWIGLU) hc[q] = t_dc[v * 8 + q][f];
-      ha[q] = t_ag[v * 8 + q][f];
-    }
-    *reinterpret_cast<uint4*>(d1T + (chunk * (P * I) + f0 + f) * 64 + v * 8) = xd;
-    if (SWIGLU) *reinterpret_cast<uint4*>(d1T + (chunk * (P * I) + I + f0 + f) * 64 + v * 8) = xc;
-    *reinterpret_cast<uint4*>(aT + (chunk * I + f0 + f) * 64 + v * 8) = xa;
   }
 }
 
@@ -322,15 +240,25 @@ __global__ void __launch_bounds__(256) grad_combine_kernel(
     __nv_bfloat16* __restrict__ du) {
   using V16 = Vec16<__nv_bfloat16>;
   constexpr int V = V16::N;
+  constexpr int kVecsPerItem = 128;  // work item: a token's 128-vector stretch
   __shared__ int s_row[8][32];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / V;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += warps) {
-    __syncwarp();
-    if (lane < k) s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
-    __syncwarp();
-    for (int v = lane; v < nvec; v += 32) {
+  const int per_tok = (nvec + kVecsPerItem - 1) / kVecsPerItem;
+  const long long items = static_cast<long long>(n_tokens) * per_tok;
+  int t_loaded = -1;
+  for (long long it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps) {
+    const int t = static_cast<int>(it / per_tok);
+    const int v0 = static_cast<int>(it % per_tok) * kVecsPerItem;
+    const int v1 = min(nvec, v0 + kVecsPerItem);
+    if (t != t_loaded) {
+      __syncwarp();
+      if (lane < k) s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
+      __syncwarp();
+      t_loaded = t;
+    }
+    for (int v = v0 + lane; v < v1; v += 32) {
       float acc[V], y[V];
       V16::load(dh + static_cast<size_t>(t) * H + v * V, acc);
       for (int j = 0; j < Ks; ++j) {
@@ -338,12 +266,23 @@ __global__ void __launch_bounds__(256) grad_combine_kernel(
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] += y[i];
       }
-      for (int s = 0; s < k; ++s) {
-        const int row = s_row[wib][s];
-        if (row < 0) continue;
-        V16::load(dx_perm + static_cast<size_t>(row) * H + v * V, y);
+      // slots in groups of 8: the group's loads are issued before any is
+      // used, then added in slot order
+      for (int s0 = 0; s0 < k; s0 += 8) {
+        uint4 raw[8];
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] += y[i];
+        for (int d = 0; d < 8; ++d) {
+          const int row = s0 + d < k ? s_row[wib][s0 + d] : -1;
+          raw[d] = row >= 0 ? __ldg(reinterpret_cast<const uint4*>(dx_perm + static_cast<size_t>(row) * H + v * V))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          if (s0 + d >= k || s_row[wib][s0 + d] < 0) continue;
+          V16::load(reinterpret_cast<const __nv_bfloat16*>(&raw[d]), y);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i] += y[i];
+        }
       }
       const float4* rr = reinterpret_cast<const float4*>(du_router + static_cast<size_t>(t) * H + v * V);
       const float4 r0 = __ldg(rr), r1 = __ldg(rr + 1);
@@ -359,20 +298,24 @@ __global__ void __launch_bounds__(256) grad_combine_kernel(
 // One block.  Per-expert segments of the weight-gradient operands:
 // seg_start[e] = Σ_{e' < e} roundup(L_e', kSegAlign) (L = rows of the expert),
 // seg_start[E] = the total.  And the two weight-gradient GEMMs' groups, their
-// k-chunk ranges and their tile prefixes (nt2 / nt13 token tiles per group):
-//   dW2 (out[n = h, m = i] over A = act rows, B = dh rows):
-//     shared j:    A chunks from j·Tpad, B chunks from 0,         Tpad / 64
-//     routed e:    A chunks from Ks·Tpad + seg, B from Tpad + seg, padded L_e / 64
-//   dW1 / dW3 (out[n = i, m = h] over A = x rows, B = dh1 rows, one group per
-//   expert and part; part 1 (up) reads dh1 rows I..2I):
-//     shared (j, part): A from 0, B from j·Tpad
-//     routed (e, part): A from Tpad + seg, B from Ks·Tpad + seg
-// Shared groups come first (their contraction is the longest).
+// contraction ranges (in rows) and their tile prefixes (nt2 / nt13 token
+// tiles per group):
+//   dW2 (out[n = h, m = i] over A = g act, B = dh rows):
+//     shared j:    g act rows from j·Tpad, dh rows from 0,              Tpad / 64 chunks
+//     routed e:    g act rows from Ks·Tpad + seg, d_perm rows from off_e, padded L_e / 64
+//   dW1 / dW3 (out[n = i, m = h] over A = x rows, B = dh1, one group per
+//   expert and part; part 1 (up) reads dh1 columns I..2I):
+//     shared (j, part): u rows from 0, dh1 rows from j·Tpad
+//     routed (e, part): x_perm rows from off_e, dh1 rows from Ks·Tpad + seg
+// Shared groups come first (their contraction is the longest).  Also the
+// input-gradient GEMM's groups (dx_groups): the forward's down-projection
+// groups fwd2 with token rows in dh1's padded row space.
 __global__ void __launch_bounds__(1024) wgrad_plan_kernel(
     const int32_t* __restrict__ offsets, int E, int Ks, int Tpad, int H, int I, int parts,
     int32_t* __restrict__ seg_start, GroupDesc* __restrict__ g2, int4* __restrict__ k2,
     GroupDesc* __restrict__ g13, int4* __restrict__ k13, int nt2, int nt13,
-    int* __restrict__ p2, int* __restrict__ p13) {
+    int* __restrict__ p2, int* __restrict__ p13, const GroupDesc* __restrict__ fwd2, int G,
+    int Tk, int T, GroupDesc* __restrict__ dx_groups) {
   __shared__ int s_seg[1025];
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
@@ -405,23 +348,44 @@ __global__ void __launch_bounds__(1024) wgrad_plan_kernel(
   // token-side width
   for (int g = threadIdx.x; g <= E + Ks; g += blockDim.x) p2[g] = g * nt2;
   for (int g = threadIdx.x; g <= (E + Ks) * parts; g += blockDim.x) p13[g] = g * nt13;
+  // Every operand is read MN-major from a row-major matrix; krange = {first
+  // row of the weight side, first row of the token side, k-chunks}.  g act
+  // and dh1 sit in the padded row space (zero rows after each expert's own);
+  // x, u, dh and d_perm are the unpadded stored rows: the rows past an
+  // expert's own that its padded contraction reaches belong to the next
+  // expert (or lie past the matrix) and meet the padding's zeros.
   constexpr int kc = 64;         // elements per k-chunk
   if (e < Ks) {
-    g2[e] = GroupDesc{0, 0, 0, 0, 1, e * H, H, 0};
-    k2[e] = make_int4(e * Tpad / kc, 0, Tpad / kc, 0);
+    // dW2: g act rows of shared expert e, dh rows from 0 (token source 1)
+    g2[e] = GroupDesc{0, 0, 1, 0, 1, e * H, H, 0};
+    k2[e] = make_int4(e * Tpad, 0, Tpad / kc, 0);
     for (int p = 0; p < parts; ++p) {
-      g13[e * parts + p] = GroupDesc{0, 0, 0, p * I, 2 + p, e * I, I, 0};
-      k13[e * parts + p] = make_int4(0, e * Tpad / kc, Tpad / kc, 0);
+      // dW1/dW3: u rows from 0 (weight-side source 1), dh1 rows of expert e
+      g13[e * parts + p] = GroupDesc{1, 0, 0, p * I, 2 + p, e * I, I, 0};
+      k13[e * parts + p] = make_int4(0, e * Tpad, Tpad / kc, 0);
     }
   }
   if (e < E) {
     const int seg = s_seg[e], n = (s_seg[e + 1] - seg) / kc;
     g2[Ks + e] = GroupDesc{0, 0, 0, 0, 0, e * H, H, 0};
-    k2[Ks + e] = make_int4((Ks * Tpad + seg) / kc, (Tpad + seg) / kc, n, 0);
+    k2[Ks + e] = make_int4(Ks * Tpad + seg, offsets[e], n, 0);
     for (int p = 0; p < parts; ++p) {
       g13[(Ks + e) * parts + p] = GroupDesc{0, 0, 0, p * I, p, e * I, I, 0};
-      k13[(Ks + e) * parts + p] = make_int4((Tpad + seg) / kc, (Ks * Tpad + seg) / kc, n, 0);
+      k13[(Ks + e) * parts + p] = make_int4(offsets[e], Ks * Tpad + seg, n, 0);
     }
+  }
+  // the input-gradient GEMM's groups: the forward's down-projection groups
+  // with their token rows moved into the padded row space of dh1
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    GroupDesc d = fwd2[g];
+    if (d.a_sel == 0) {            // routed expert a_row0 / H, from its first row
+      const int ex = d.a_row0 / H;
+      d.b_row0 = Ks * Tpad + s_seg[ex] + (d.b_row0 - offsets[ex]);
+    } else {                       // shared expert j's piece from token p0
+      const int rel = d.b_row0 - Tk, j = rel / T;
+      d.b_row0 = j * Tpad + (rel - j * T);
+    }
+    dx_groups[g] = d;
   }
 }
 

@@ -8,9 +8,10 @@
 
 // Workspace of the layer backward.  Rall = T·k + Ks·T expert input rows
 // (routed rows, then each shared expert's T rows); P = 2 (SwiGLU) or 1 (ReLU)
-// pre-activation blocks per row.  The weight-gradient operands are K-major
-// copies with the shared experts' T rows first (padded to Tpad) and then
-// each routed expert's rows (padded to kSegAlign).
+// pre-activation blocks per row.  The K-major weight-gradient operands
+// (g act)ᵀ and dh1ᵀ hold the shared experts' T rows first (each padded to
+// Tpad) and then each routed expert's rows (padded to kSegAlign); KX is the
+// padded extent of one shared block plus all routed segments.
 struct BwdWs {
   float* logits;
   int32_t* idx;
@@ -24,7 +25,7 @@ struct BwdWs {
   int* tile_prefix;
   __nv_bfloat16 *x_perm, *d_perm;        // [Tk, H]
   __nv_bfloat16 *a, *c, *dm;             // [Rall, I]
-  __nv_bfloat16* dh1;                    // [Rall, P·I]
+  __nv_bfloat16* dh1p;                   // [KA, P·I]: padded row space
   float* row_gate;                       // [Tk]
   float* dg_part;                        // [Tk, I / 64]: <dm, act> per 64-feature block
   __nv_bfloat16* dz;                     // [T, Epad], zeros past E
@@ -35,8 +36,8 @@ struct BwdWs {
   GroupDesc *wg2, *wg13;
   int4 *wk2, *wk13;
   int *wp2, *wp13;
-  __nv_bfloat16 *xT, *dT;                // [H, KX]
-  __nv_bfloat16 *aT, *d1T;               // [I, KA], [P·I, KA]
+  __nv_bfloat16* gactp;                  // [KA, I]: g act, padded row space
+  GroupDesc* dxg;                        // the input-gradient GEMM's groups
   long long Tpad, KX, KA;
   size_t total;
 };
@@ -79,7 +80,7 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.a = bf(Rall * I);
   B.c = P == 2 ? bf(Rall * I) : nullptr;
   B.dm = bf(Rall * I);
-  B.dh1 = bf(Rall * P * I);
+
   B.row_gate = static_cast<float*>(take(Tk * 4));
   B.dg_part = static_cast<float*>(take(Tk * (I / 64) * 4));
   B.Epad = static_cast<int>((E + tc::kBK - 1) / tc::kBK * tc::kBK);
@@ -95,10 +96,9 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.wg13 = static_cast<GroupDesc*>(take(G13 * sizeof(GroupDesc)));
   B.wk13 = static_cast<int4*>(take(G13 * sizeof(int4)));
   B.wp13 = static_cast<int*>(take((G13 + 1) * 4));
-  B.xT = bf(H * static_cast<size_t>(B.KX));
-  B.dT = bf(H * static_cast<size_t>(B.KX));
-  B.aT = bf(I * static_cast<size_t>(B.KA));
-  B.d1T = bf(P * I * static_cast<size_t>(B.KA));
+  B.dh1p = bf(P * I * static_cast<size_t>(B.KA));
+  B.gactp = bf(I * static_cast<size_t>(B.KA));
+  B.dxg = static_cast<GroupDesc*>(take(G * sizeof(GroupDesc)));
   B.total = off;
   return B;
 }
@@ -113,21 +113,6 @@ moe_status check_backward(const moe_shape* s) {
 
 MOE_API size_t moe_layer_backward_workspace_size(const moe_shape* s) {
   return check_backward(s) == MOE_OK ? carve_bwd(nullptr, s).total : 0;
-}
-
-// Token rows into the chunk-major K-major weight-gradient operands (cols
-// rows of features): rows [0, n) of src (row pitch = cols) into dst columns
-// [col0, col0 + roundup(n, 64)), zeros past n; with seg_start, the routed
-// rows into per-expert segments.
-moe_status transpose_rows(const __nv_bfloat16* src, int cols, int n, const int32_t* seg_start,
-                          const int32_t* offsets, int E, int max_cols, __nv_bfloat16* dst,
-                          long long col0, cudaStream_t st) {
-  if (max_cols <= 0) return MOE_OK;
-  if (cols % 64 || col0 % 64 || !al16(src) || !al16(dst)) return MOE_ERR_INVALID_ARG;
-  dim3 grid(cdiv(max_cols, 64), cols / 64, 1);
-  transpose_kernel<<<grid, 256, 0, st>>>(src, cols, n, seg_start, offsets, E, dst, col0);
-  MOE_CUDA(cudaGetLastError());
-  return MOE_OK;
 }
 
 moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void* u,
@@ -210,7 +195,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   const int nt2 = cdiv(H, 256), nt13 = cdiv(I, 256);
   wgrad_plan_kernel<<<1, 1024, 0, st>>>(B.offsets, E, Ks, static_cast<int>(B.Tpad), H, I, P,
                                         B.seg_start, B.wg2, B.wk2, B.wg13, B.wk13, nt2, nt13,
-                                        B.wp2, B.wp13);
+                                        B.wp2, B.wp13, B.g2, G, Tk, T, B.dxg);
   MOE_CUDA(cudaGetLastError());
   const int rmax = static_cast<int>(B.KX - B.Tpad);
   const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
@@ -271,12 +256,12 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
                        long long col0) -> moe_status {
       if (swiglu)
         act_backward_kernel<true><<<grid, 256, 0, st>>>(
-            B.a, B.c, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E, B.dh1,
-            B.d1T, B.aT, col0, B.dg_part);
+            B.a, B.c, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
+            B.dh1p, B.gactp, col0, B.dg_part);
       else
         act_backward_kernel<false><<<grid, 256, 0, st>>>(
             B.a, nullptr, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
-            B.dh1, B.d1T, B.aT, col0, B.dg_part);
+            B.dh1p, B.gactp, col0, B.dg_part);
       MOE_CUDA(cudaGetLastError());
       return MOE_OK;
     };
@@ -325,11 +310,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     MOE_TRY(make_out_map_f32(&p.omap32[0], B.du_router, T, H));
     p.omap32[1] = p.omap32[0];
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
-    // d_centroids = dzᵀ u: dz [T, Epad] read MN-major (M = experts), uᵀ from
-    // the chunk-major copy of the shared experts' operand (K = T, padded
-    // with zeros to Tpad); stored transposed into [E, H]
-    MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(u), H, T, nullptr, nullptr, 0,
-                           static_cast<int>(B.Tpad), B.xT, 0, st));
+    // d_centroids = dzᵀ u: dz [T, Epad] read MN-major (M = experts), u [T, H]
+    // read MN-major (N = H; K = T, rows past T zero-filled); stored
+    // transposed into [E, H]
     tc::Params q;
     memset(&q, 0, sizeof(q));
     MOE_TRY(make_map3_mn(&q.a[0], B.dz, T, Epad));
@@ -337,8 +320,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     q.a_mn = 1;
     q.a_mn_per_expert = Epad;
     q.a_k_per_expert = T;
-    MOE_TRY(make_token_maps_chunked(q.b[0], B.xT, H, B.KX / 64));
-    memcpy(q.b[1], q.b[0], sizeof(q.b[0]));
+    MOE_TRY(make_map3_mn(&q.b[0][0], u, T, H));
+    q.b[1][0] = q.b[0][0];
+    q.b_mn = 1;
     q.dense_count = H;
     q.n_wtiles = cdiv(Epad, 256);
     q.num_k_blocks = static_cast<int>(B.Tpad / tc::kBK);
@@ -375,9 +359,9 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
       if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wt->sw1, static_cast<uint64_t>(Ks) * I, H));
       else p.a[1] = p.a[0];
     }
-    MOE_TRY(make_token_maps(p.b[0], B.dh1, Rall, PI));
+    MOE_TRY(make_token_maps(p.b[0], B.dh1p, B.KA, PI));
     memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
-    p.groups = B.g2;
+    p.groups = B.dxg;
     p.tile_prefix = B.tile_prefix;
     p.n_groups = G;
     p.n_wtiles = cdiv(H, tc::kBM * pair);
@@ -392,25 +376,29 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     p.out_cols = H;
     MOE_TRY(launch_ffn<tc::EPI_BF16>(p, bn, st));
   }
-  grad_combine_kernel<<<route_blocks(T), 256, 0, st>>>(
+  const int gc_blocks = one_wave_blocks(grad_combine_kernel, 256);
+  if (gc_blocks <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+  grad_combine_kernel<<<gc_blocks, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(dh), B.dx_perm, B.dx_sh, B.slot_row, B.du_router, T, H,
       k, Ks, static_cast<__nv_bfloat16*>(du));
   MOE_CUDA(cudaGetLastError());
 
-  // ---- weight gradients: contractions over each expert's own rows
-  MOE_TRY(transpose_rows(static_cast<const __nv_bfloat16*>(dh), H, T, nullptr, nullptr, 0,
-                         static_cast<int>(tpad), B.dT, 0, st));
-  if (Tk > 0) {
-    MOE_TRY(transpose_rows(B.x_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.xT, tpad, st));
-    MOE_TRY(transpose_rows(B.d_perm, H, Tk, B.seg_start, B.offsets, E, rmax, B.dT, tpad, st));
-  }
+  // ---- weight gradients: contractions over each expert's own rows; the
+  // row-major operands (dh and x rows) are read MN-major where they are
   {  // dW2[e][h][i] = Σ_r dh_r[h] · (g act)_r[i]
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3_chunked(&p.a[0], B.aT, I, B.KA / 64, tc::kBM));
+    MOE_TRY(make_map3_mn(&p.a[0], B.gactp, B.KA, I));
     p.a[1] = p.a[0];
-    MOE_TRY(make_token_maps_chunked(p.b[0], B.dT, H, B.KX / 64));
-    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    p.a_mn = 1;
+    p.a_k_rows = 1;
+    p.a_mn_per_expert = I;   // every group's M range starts at 0: no per-expert offset
+    p.a_k_per_expert = 0;
+    MOE_TRY(make_map3_mn(&p.b[1][0], dh, T, H));
+    if (Tk > 0) MOE_TRY(make_map3_mn(&p.b[0][0], B.d_perm, Tk, H));
+    else p.b[0][0] = p.b[1][0];
+    p.b_mn = 1;
+    p.b_k_rows = 1;
     p.groups = B.wg2;
     p.tile_prefix = B.wp2;
     p.krange = B.wk2;
@@ -429,10 +417,17 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   {  // dW1[e][i][h] = Σ_r da_r[i] · x_r[h], dW3 likewise with dc
     tc::Params p;
     memset(&p, 0, sizeof(p));
-    MOE_TRY(make_map3_chunked(&p.a[0], B.xT, H, B.KX / 64, tc::kBM));
-    p.a[1] = p.a[0];
-    MOE_TRY(make_token_maps_chunked(p.b[0], B.d1T, PI, B.KA / 64));
-    memcpy(p.b[1], p.b[0], sizeof(p.b[0]));
+    MOE_TRY(make_map3_mn(&p.a[1], u, T, H));
+    if (Tk > 0) MOE_TRY(make_map3_mn(&p.a[0], B.x_perm, Tk, H));
+    else p.a[0] = p.a[1];
+    p.a_mn = 1;
+    p.a_k_rows = 1;
+    p.a_mn_per_expert = H;   // every group's M range starts at 0: expert 0, no k offset
+    p.a_k_per_expert = 0;
+    MOE_TRY(make_map3_mn(&p.b[0][0], B.dh1p, B.KA, PI));
+    p.b[1][0] = p.b[0][0];
+    p.b_mn = 1;
+    p.b_k_rows = 1;
     p.groups = B.wg13;
     p.tile_prefix = B.wp13;
     p.krange = B.wk13;

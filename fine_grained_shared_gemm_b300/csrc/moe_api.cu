@@ -138,17 +138,6 @@ moe_status make_map3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
   return encode(m, 3, base, dims, strides, box);
 }
 
-// Chunk-major bf16 operand (element (r, k) at ((k / 64) · rows + r) · 64 + k % 64,
-// n_chunks chunks of 64 columns): the same (64 columns, rows, chunks) view
-// as make_map3, with each chunk a contiguous block of rows x 128 bytes.
-moe_status make_map3_chunked(CUtensorMap* m, const void* base, uint64_t rows, uint64_t n_chunks,
-                             uint32_t box_rows) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::kBK), rows, n_chunks};
-  const cuuint64_t strides[2] = {tc::kBK * 2, rows * tc::kBK * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(tc::kBK), box_rows, tc::kKPS};
-  return encode(m, 3, base, dims, strides, box);
-}
-
 // A weight stack bf16 [rows, cols] row-major read MN-major (the operand is its
 // transpose): (64 columns, rows, cols / 64 column blocks), box 64 columns x
 // kKPS·64 rows x 2 column blocks, landing [block][row][64] (two slabs).
@@ -220,12 +209,6 @@ moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, u
   return MOE_OK;
 }
 
-moe_status make_token_maps_chunked(CUtensorMap* maps, const void* base, uint64_t rows,
-                                   uint64_t n_chunks) {
-  for (int i = 0; i < tc::kNumBoxes; ++i)
-    MOE_TRY(make_map3_chunked(&maps[i], base, rows, n_chunks, 16u << i));
-  return MOE_OK;
-}
 
 // Launches the grouped GEMM persistently: one CTA per SM, or for PAIR == 2
 // as many two-CTA clusters as fit on the device at once (at most max_ctas
@@ -397,6 +380,23 @@ LayerWs carve_layer(void* ws, const moe_shape* s) {
 // ---------------------------------------------------------------- steps
 
 int route_blocks(int T) { return std::max(1, std::min(cdiv(T, 8), num_sms() * 8)); }
+
+// Blocks of `threads` that are resident on the device at once (one wave) for
+// a kernel without dynamic shared memory; cached per kernel and device.
+template <typename K>
+int one_wave_blocks(K kernel, int threads) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
+            cudaSuccess || per_sm <= 0)
+      return 0;
+    cached[dev] = per_sm * num_sms();
+  }
+  return cached[dev];
+}
 
 moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
                             const float* off, float* logits, cudaStream_t st) {
@@ -631,8 +631,11 @@ moe_status do_combine(const moe_shape* s, const void* u, const void* y_perm,
                       cudaStream_t st) {
   const int T = s->T;
   if (T == 0) return MOE_OK;
-  const int blocks = route_blocks(T);
-  if (s->dtype == MOE_DTYPE_F32)
+  const bool f32 = s->dtype == MOE_DTYPE_F32;
+  const int blocks = f32 ? one_wave_blocks(combine_kernel<float>, 256)
+                         : one_wave_blocks(combine_kernel<__nv_bfloat16>, 256);
+  if (blocks <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+  if (f32)
     combine_kernel<float><<<blocks, 256, 0, st>>>(
         static_cast<const float*>(u), static_cast<const float*>(y_perm),
         static_cast<const float*>(y_shared), w, slot_row, T, s->H, s->top_k, s->n_shared,

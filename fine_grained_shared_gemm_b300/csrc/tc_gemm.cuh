@@ -95,6 +95,18 @@ struct Params {
   int a_k_per_expert;
   int a_stack_chunks;
   int a_stack_swap[2];           // per weight stack (routed, shared)
+  // With a_mn == 1, a_k_rows: the weight operand's k runs over rows of its
+  // stored matrix starting at row krange.x (a row, not a k-chunk), so a
+  // group's contraction can start at any row.
+  int a_k_rows;
+  // Token operand MN-major (b_mn): the token side is read in its stored
+  // row-major layout as the transpose of the operand — operand element
+  // (n, k) at row k, column n — through maps (64 columns, rows, column
+  // blocks of 64) with a box of 64 columns x kKPS·64 rows x 2 blocks; every
+  // tile is BN columns wide (columns past the matrix are zero-filled, only
+  // the valid ones are stored).  b_k_rows: k starts at row krange.y.
+  int b_mn;
+  int b_k_rows;
   CUtensorMap b[2][kNumBoxes];   // token sources x box heights: 3-D
   const GroupDesc* groups;       // [n_groups], or null for one dense group
   const int* tile_prefix;        // [n_groups + 1] prefix sum of token tiles
@@ -414,10 +426,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t slab
          (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, B K-major, A
-// K-major or (a_mn) MN-major.  m is the MMA's full M (256 for a CTA pair).
-__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn = 0) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | ((n >> 3) << 17) |
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, each operand
+// K-major or (a_mn, b_mn) MN-major.  m is the MMA's full M (256 for a CTA pair).
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n, uint32_t a_mn = 0,
+                                               uint32_t b_mn = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
          ((m >> 4) << 24);
 }
 
@@ -587,6 +600,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.n_valid = min(th, d.count - n * th);
   tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
   tl.nt = nt;
+  if (p.b_mn) tl.n_mma = BN;  // MN-major tokens: whole 64-column blocks per CTA
   tl.b_rows = tl.n_mma / PAIR;
   tl.b_box = box_index(tl.b_rows);
   tl.b_src = d.b_src;
@@ -676,7 +690,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int t = first; t < total && ok; t += stride) {
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
         const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
-        const int b_land = 16 << tl.b_box;  // token rows each CTA's copy lands per k-block
+        // token rows each CTA's copy lands per k-block (MN-major: BN / PAIR
+        // columns, the same bytes)
+        const int b_land = p.b_mn ? C::kBRows : 16 << tl.b_box;
         // bytes both CTAs' copies deliver to the leader's barrier per stage
         const uint32_t bytes =
             static_cast<uint32_t>(PAIR * kKPS) * (kABytes + static_cast<uint32_t>(b_land) * (kBK * 2));
@@ -706,7 +722,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                               pol_a);
           } else if (p.a_mn == 1) {
             // 128 k rows x two 64-column blocks: [block][row][64]
-            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, a_k0 + (tl.ka0 + kb) * kBK, a_mb, pol_a);
+            const int row = p.a_k_rows ? tl.ka0 + kb * kBK : a_k0 + (tl.ka0 + kb) * kBK;
+            tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, row, a_mb, pol_a);
           } else if (p.a_mn == 2) {
             const int c = tl.ka0 + kb;  // k-chunk pairs never straddle the two stacks
             const int stack = (c >= p.a_stack_chunks) != (p.a_stack_swap[tl.a_sel] != 0) ? 1 : 0;
@@ -716,7 +733,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tma_load_3d<PAIR>(sa, &p.a[tl.a_sel], fb, 0, tl.a_row, tl.ka0 + kb, pol_a);
           }
           // tokens: both k-blocks in one copy
-          tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, tl.kb0 + kb, pol_keep);
+          if (p.b_mn) {
+            const int row = p.b_k_rows ? tl.kb0 + kb * kBK : (tl.kb0 + kb) * kBK;
+            tma_load_3d<PAIR>(sa + kKPS * kABytes, &p.b[tl.b_src][0], fb, 0, row, tl.b_row / 64,
+                              pol_keep);
+          } else {
+            tma_load_3d<PAIR>(sa + kKPS * kABytes, bmap, fb, 0, tl.b_row, tl.kb0 + kb, pol_keep);
+          }
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -746,7 +769,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a0 * BN);
         const uint32_t idesc =
-            idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma), p.a_mn != 0 ? 1u : 0u);
+            idesc_bf16(kBM * PAIR, static_cast<uint32_t>(tl.n_mma), p.a_mn != 0 ? 1u : 0u,
+                       p.b_mn != 0 ? 1u : 0u);
         const uint32_t boff = static_cast<uint32_t>(16 << tl.b_box) * (kBK * 2);
         for (int kb = 0; kb < tl.nk; kb += kKPS) {
           if (!mbar_wait(full_bar(stage), phase)) {
@@ -766,10 +790,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint64_t da = p.a_mn ? sdesc_sw128_mn(sa + c * (kBK * 128), kKPS * kBK * 128)
                                        : sdesc_sw128(sa + c * kABytes);
             const uint32_t a_step = p.a_mn ? (kUmmaK * 128) >> 4 : 2;
-            const uint64_t db = sdesc_sw128(sa + kKPS * kABytes + c * boff);
+            // K-major B: k-block c is boff bytes further; MN-major B: like
+            // MN-major A (two slabs of kKPS·64 rows, k-block c 64 rows in)
+            const uint64_t db = p.b_mn ? sdesc_sw128_mn(sa + kKPS * kABytes + c * (kBK * 128),
+                                                         kKPS * kBK * 128)
+                                       : sdesc_sw128(sa + kKPS * kABytes + c * boff);
+            const uint32_t b_step = p.b_mn ? (kUmmaK * 128) >> 4 : 2;
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              tc_mma<PAIR>(d_tmem, da + a_step * k, db + 2 * k, idesc, ((kb + c) | k) != 0);
+              tc_mma<PAIR>(d_tmem, da + a_step * k, db + b_step * k, idesc, ((kb + c) | k) != 0);
           }
           tc_commit_all<PAIR>(empty_bar(stage));  // frees the stage in both CTAs once read
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -914,20 +943,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const float up = gate_warp ? pv[i] : __uint_as_float(v[16 + i]);
             return silu_tanh(g) * up;
           }, gate_warp ? 0 : 16, (q & 1) * 32);
-          if (gate_warp && p.save)  // the gate pre-activation too, for a later backward
-            emit_to(&p.save_map[0], p.save_out[0],
+          // in the training forward each warp also stores the pre-activation
+          // it holds (gate or up, same output columns as its partner's) for a
+          // later backward
+          if (p.save)
+            emit_to(&p.save_map[gate_warp ? 0 : 1], p.save_out[gate_warp ? 0 : 1],
                     [&](int j) { return __uint_as_float(v[j]); }, (q & 1) * 32);
-          else if (p.save && cols_ok) {
-            // the up warp stores the up pre-activation it holds (same output
-            // columns as its partner's): 64 contiguous bytes per token row
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.save_out[1]) +
-                               static_cast<size_t>(tl.out_row + c0) * p.out_ld + tl.out_col +
-                               (q & 1) * 32 + lane;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nrow)
-                o[static_cast<size_t>(j) * p.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          }
         } else if (EPI == EPI_F32) {
           // lane = output column: for each token row j the warp writes 32
           // consecutive fp32 columns (128 bytes) of that row
