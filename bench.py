@@ -280,8 +280,10 @@ class ClockSampler:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
                     "error": self.error}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples),
+                "sm_mhz_mean": round(statistics.fmean(self.samples), 1),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
 
 
 class Layer:
@@ -335,9 +337,10 @@ def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
         n += (2 if sw else 1) if rows else 0      # pre-activations recomputed
     n += 2 if k else 0                            # scatter dh rows, row gate weights
     n += 2                                        # FFN plan, weight-gradient plan
-    n += 1 if rows else 0                         # dm = dh W2
-    n += s.n_shared + (1 if k else 0)             # activation derivative
-    n += 1 + 2                                    # gate, router GEMMs
+    n += 1 if rows else 0                         # dm = dh W2 (SwiGLU: + derivative)
+    if not sw:
+        n += s.n_shared + (1 if k else 0)         # ReLU derivative
+    n += 1 + 2 + 1                                # gate, router GEMMs, partial sums
     n += (1 if rows else 0) + 1                   # dx, du
     n += 2                                        # weight-gradient GEMMs
     return n
@@ -374,12 +377,13 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    for i in range(K):
-        flush.zero_()
-        ev[i][0].record()
-        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws)
-        ev[i][1].record()
-    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk_b:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record()
+            M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws)
+            ev[i][1].record()
+        torch.cuda.synchronize()
     st, code = M.moe_device_status()
     if st != M.MOE_OK:
         raise RuntimeError(f"device status {st} code {code} in the backward")
@@ -398,22 +402,53 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
             for _ in range(K)]
     ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(K)]
-    for i in range(K):
-        flush.zero_()
-        ev_f[i][0].record()
-        M.moe_layer_forward_train(s, layer.wt, inp.u, h, saved, layer.ws_l)
-        ev_f[i][1].record()
-        flush.zero_()
-        ev_b[i][0].record()
-        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws, saved=saved)
-        ev_b[i][1].record()
-    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk_t:
+        for i in range(K):
+            flush.zero_()
+            ev_f[i][0].record()
+            M.moe_layer_forward_train(s, layer.wt, inp.u, h, saved, layer.ws_l)
+            ev_f[i][1].record()
+            flush.zero_()
+            ev_b[i][0].record()
+            M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws, saved=saved)
+            ev_b[i][1].record()
+        torch.cuda.synchronize()
     st, code = M.moe_device_status()
     if st != M.MOE_OK:
         raise RuntimeError(f"device status {st} code {code} in the training step")
     f_ms = sum(a.elapsed_time(b) for a, b in ev_f) / K
     b_ms = sum(a.elapsed_time(b) for a, b in ev_b) / K
     step_flops = expert_flops(s) + 2 * s.T * E * H + flops
+    # the same two calls captured once into CUDA graphs and replayed, as a
+    # training loop over fixed shapes runs them (the same kernels; the graph
+    # saves the per-launch host and launch-processing time)
+    g_f, g_b = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_f):
+        M.moe_layer_forward_train(s, layer.wt, inp.u, h, saved, layer.ws_l)
+    with torch.cuda.graph(g_b):
+        M.moe_layer_backward(s, layer.wt, inp.u, dh, du, grads, ws, saved=saved)
+    for _ in range(args.warmup):
+        g_f.replay()
+        g_b.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk_g:
+        for i in range(K):
+            flush.zero_()
+            ev_f[i][0].record()
+            g_f.replay()
+            ev_f[i][1].record()
+            flush.zero_()
+            ev_b[i][0].record()
+            g_b.replay()
+            ev_b[i][1].record()
+        torch.cuda.synchronize()
+    st, code = M.moe_device_status()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status {st} code {code} in the graph-replayed training step")
+    gf_ms = sum(a.elapsed_time(b) for a, b in ev_f) / K
+    gb_ms = sum(a.elapsed_time(b) for a, b in ev_b) / K
+    del g_f, g_b
     del ws, g, grads, saved
     return {"tokens_per_s": round(s.T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
             "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
@@ -421,12 +456,21 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
             "gpu_launches": backward_launches(s) * K,
             "note": "recomputes routing and the gate/up pre-activations from u; "
                     "weight gradients fp32",
+            "clocks": clk_b.summary(),
             "training_step": {
                 "forward_train_ms": round(f_ms, 4), "backward_saved_ms": round(b_ms, 4),
                 "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
                 "tokens_per_s": round(s.T / ((f_ms + b_ms) / 1e3), 1),
                 "tflops": round(step_flops / ((f_ms + b_ms) / 1e3) / 1e12, 1),
-                "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"}}
+                "clocks": clk_t.summary(),
+                "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"},
+            "training_step_graph": {
+                "forward_train_ms": round(gf_ms, 4), "backward_saved_ms": round(gb_ms, 4),
+                "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
+                "tokens_per_s": round(s.T / ((gf_ms + gb_ms) / 1e3), 1),
+                "tflops": round(step_flops / ((gf_ms + gb_ms) / 1e3) / 1e12, 1),
+                "clocks": clk_g.summary(),
+                "note": "the same two calls, each captured into a CUDA graph and replayed"}}
 
 
 def measure_forward(args, shape, dev, flush, world, peaks, barrier):

@@ -9,15 +9,19 @@
 // GEMMs read the weights MN-major, in their stored layout; the weight
 // gradients read the token rows x, dh and u MN-major, in theirs); the kernels
 // here produce its other operands and consume its outputs:
-//   act_backward_kernel    SwiGLU / ReLU derivative per row, written row-major
-//                          and K-major (chunk-major, each expert's rows
-//                          padded with zeros to kSegAlign: the weight
-//                          gradients contract over each expert's own rows),
-//                          the gate-scaled activation (K-major, for dW2) and
-//                          the per-row <dy, y> for the gate gradient
+//   row_gate_kernel        each routed row's gate weight
+//   relu_backward_kernel   ReLU derivative per row and the gate-scaled
+//                          activation, written row-major into a padded row
+//                          space (each expert's rows padded with zero rows:
+//                          the weight gradients contract over each expert's
+//                          own rows), and the per-row <dy, y> for the gate
+//                          gradient (for SwiGLU the dm GEMM's epilogue
+//                          computes the same)
 //   gate_backward_kernel   dL/dz from dL/dg through softmax or the normalised
 //                          sigmoid (dz · centroids and dzᵀ · u are grouped
 //                          GEMMs too)
+//   sum_partials_kernel    adds the contraction ranges' partial sums of
+//                          dzᵀ · u in range order
 //   grad_combine_kernel    du = dh + Σ shared dx + Σ slot dx + router term
 //   wgrad_plan_kernel      padded per-expert segments and the weight-gradient
 //                          GEMMs' groups
@@ -37,34 +41,31 @@ constexpr int kSegAlign = 128;
 
 // ---------------------------------------------------------------- per-row derivative
 
-// For row r of the expert inputs (routed rows [0, Tk), then shared rows) with
-// a = x W1ᵀ, c = x W3ᵀ (SwiGLU) and dm = dh W2 for the row's token (NOT yet
+// For row r of the expert inputs (routed rows [0, Tk), then shared rows) of a
+// ReLU layer with a = x W1ᵀ and dm = dh W2 for the row's token (NOT yet
 // scaled by the row's gate weight g; g = 1 for shared rows):
-//   dh1[r]  = [g dm ⊙ c ⊙ SiLU'(a) | g dm ⊙ SiLU(a)]   (SwiGLU, 2I wide)
-//           = g dm ⊙ [a > 0]                            (ReLU, I wide)
-//   g act   with act = SiLU(a) ⊙ c, or ReLU(a)
+//   dh1[r]  = g dm ⊙ [a > 0]
+//   g act   with act = ReLU(a)
 //   <dm, act> (= dL/dg of the row)
-// SiLU'(a) = σ(a) (1 + a (1 − σ(a))).  One block per 64 rows x 64 features.
-// dh1 and g act are written row-major into the padded row space the
-// weight-gradient and input-gradient GEMMs read: each shared expert's T rows
-// padded with zero rows to Tpad, then each routed expert's rows padded with
-// zero rows to kSegAlign (dh1p [KA, P·I], gactp [KA, I]; the block's padded
-// rows start at prow0 + blockIdx.x · 64).  The block's source rows: a run of
-// rows_total rows from row_base (seg_start == nullptr; row(j) = row_base +
-// j), or the routed rows by expert segment (expert e owns padded rows
-// [seg_start[e], seg_start[e+1]) of the routed region and row(j) =
-// offsets[e] + j - seg_start[e] while that is below offsets[e+1]); padded
-// rows with no source row are written as zeros.  The 64 features' share of
-// <dm, act> goes to dg_part[r · (I / 64) + blockIdx.y] (routed rows only),
-// summed later in block order.
-template <bool SWIGLU>
-__global__ void __launch_bounds__(256) act_backward_kernel(
-    const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ c,
-    const __nv_bfloat16* __restrict__ dm, const float* __restrict__ row_gate, long long Tk,
-    int I, long long row_base, int rows_total, const int32_t* __restrict__ seg_start,
-    const int32_t* __restrict__ offsets, int E, __nv_bfloat16* __restrict__ dh1p,
-    __nv_bfloat16* __restrict__ gactp, long long prow0, float* __restrict__ dg_part) {
-  constexpr int P = SWIGLU ? 2 : 1;
+// (A SwiGLU layer gets the same quantities from the dm GEMM's epilogue.)
+// One block per 64 rows x 64 features.  dh1 and g act are written row-major
+// into the padded row space the weight-gradient and input-gradient GEMMs
+// read: each shared expert's T rows padded with zero rows to Tpad, then each
+// routed expert's rows padded with zero rows to kSegAlign (dh1p [KA, I],
+// gactp [KA, I]; the block's padded rows start at prow0 + blockIdx.x · 64).
+// The block's source rows: a run of rows_total rows from row_base (seg_start
+// == nullptr; row(j) = row_base + j), or the routed rows by expert segment
+// (expert e owns padded rows [seg_start[e], seg_start[e+1]) of the routed
+// region and row(j) = offsets[e] + j - seg_start[e] while that is below
+// offsets[e+1]); padded rows with no source row are written as zeros.  The
+// 64 features' share of <dm, act> goes to dg_part[r · (I / 64) + blockIdx.y]
+// (routed rows only), summed later in block order.
+__global__ void __launch_bounds__(256) relu_backward_kernel(
+    const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ dm,
+    const float* __restrict__ row_gate, long long Tk, int I, long long row_base, int rows_total,
+    const int32_t* __restrict__ seg_start, const int32_t* __restrict__ offsets, int E,
+    __nv_bfloat16* __restrict__ dh1p, __nv_bfloat16* __restrict__ gactp, long long prow0,
+    float* __restrict__ dg_part) {
   const int j0 = blockIdx.x * 64;
   const int f0 = blockIdx.y * 64;
   const int nb = I / 64;
@@ -86,42 +87,28 @@ __global__ void __launch_bounds__(256) act_backward_kernel(
   }
   for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {   // two (row, 8 features) per thread
     const int r = i >> 3, v = i & 7;
-    float da[8], dc[8], ag[8];
+    float da[8], ag[8];
     float dot = 0.0f;
     if (r < valid) {
       const long long R = row0 + r;
       const float g = R < Tk ? __ldg(row_gate + R) : 1.0f;
       const size_t off = static_cast<size_t>(R) * I + f0 + v * 8;
-      float fa[8], fc[8], fd[8];
+      float fa[8], fd[8];
       Vec16<__nv_bfloat16>::load(a + off, fa);
       Vec16<__nv_bfloat16>::load(dm + off, fd);
-      if (SWIGLU) Vec16<__nv_bfloat16>::load(c + off, fc);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        if (SWIGLU) {
-          const float sg = 1.0f / (1.0f + expf(-fa[q]));
-          const float si = fa[q] * sg;
-          const float act = si * fc[q];
-          dot = fmaf(fd[q], act, dot);
-          const float gd = g * fd[q];
-          da[q] = gd * fc[q] * sg * (1.0f + fa[q] * (1.0f - sg));
-          dc[q] = gd * si;
-          ag[q] = g * act;
-        } else {
-          const float act = fmaxf(fa[q], 0.0f);
-          dot = fmaf(fd[q], act, dot);
-          da[q] = fa[q] > 0.0f ? g * fd[q] : 0.0f;
-          dc[q] = 0.0f;
-          ag[q] = g * act;
-        }
+        const float act = fmaxf(fa[q], 0.0f);
+        dot = fmaf(fd[q], act, dot);
+        da[q] = fa[q] > 0.0f ? g * fd[q] : 0.0f;
+        ag[q] = g * act;
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) da[q] = dc[q] = ag[q] = 0.0f;
+      for (int q = 0; q < 8; ++q) da[q] = ag[q] = 0.0f;
     }
     const size_t prow = static_cast<size_t>(prow0 + j0 + r);
-    Vec16<__nv_bfloat16>::store(dh1p + prow * (P * I) + f0 + v * 8, da);
-    if (SWIGLU) Vec16<__nv_bfloat16>::store(dh1p + prow * (P * I) + I + f0 + v * 8, dc);
+    Vec16<__nv_bfloat16>::store(dh1p + prow * I + f0 + v * 8, da);
     Vec16<__nv_bfloat16>::store(gactp + prow * I + f0 + v * 8, ag);
     // the row's 8 vectors sit in 8 consecutive lanes: add them in a fixed order
     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
@@ -230,6 +217,24 @@ __global__ void __launch_bounds__(256) gate_backward_kernel(
 
 // ---------------------------------------------------------------- du
 
+// out[i] = Σ_{s<S} part[s · n4 + i] over float4 elements, s in order (a fixed
+// summation order, so the result does not depend on scheduling).
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float4* __restrict__ part,
+                                                           int S, long long n4,
+                                                           float4* __restrict__ out) {
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += gridDim.x * 256LL) {
+    float4 acc = __ldg(part + i);
+    for (int sp = 1; sp < S; ++sp) {
+      const float4 v = __ldg(part + sp * n4 + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    out[i] = acc;
+  }
+}
+
 // du_t = dh_t + Σ_{j<Ks} dx_shared[j, t] + Σ_{s<k} dx_perm[slot_row[t, s]] + du_router_t,
 // fp32 in this order, one rounding to bf16.  The routed rows were computed
 // from gate-scaled upstream gradients, so they add with weight 1.
@@ -309,13 +314,16 @@ __global__ void __launch_bounds__(256) grad_combine_kernel(
 //     routed (e, part): x_perm rows from off_e, dh1 rows from Ks·Tpad + seg
 // Shared groups come first (their contraction is the longest).  Also the
 // input-gradient GEMM's groups (dx_groups): the forward's down-projection
-// groups fwd2 with token rows in dh1's padded row space.
+// groups fwd2 with token rows in dh1's padded row space; and the fused
+// dm GEMM's groups (dm_groups): the forward's gate/up groups fwd1 with their
+// first padded row in GroupDesc.pad.
 __global__ void __launch_bounds__(1024) wgrad_plan_kernel(
     const int32_t* __restrict__ offsets, int E, int Ks, int Tpad, int H, int I, int parts,
     int32_t* __restrict__ seg_start, GroupDesc* __restrict__ g2, int4* __restrict__ k2,
     GroupDesc* __restrict__ g13, int4* __restrict__ k13, int nt2, int nt13,
     int* __restrict__ p2, int* __restrict__ p13, const GroupDesc* __restrict__ fwd2, int G,
-    int Tk, int T, GroupDesc* __restrict__ dx_groups) {
+    int Tk, int T, GroupDesc* __restrict__ dx_groups, const GroupDesc* __restrict__ fwd1,
+    GroupDesc* __restrict__ dm_groups) {
   __shared__ int s_seg[1025];
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
@@ -386,6 +394,16 @@ __global__ void __launch_bounds__(1024) wgrad_plan_kernel(
       d.b_row0 = j * Tpad + (rel - j * T);
     }
     dx_groups[g] = d;
+    // the fused dm GEMM's groups: the forward's gate/up groups (output rows
+    // = the rows of a and c), each with its first row in the padded space
+    GroupDesc d1 = fwd1[g];
+    if (d1.a_sel == 0) {           // routed expert a_row0 / I, from its first row
+      const int ex = d1.a_row0 / I;
+      d1.pad = Ks * Tpad + s_seg[ex] + (d1.b_row0 - offsets[ex]);
+    } else {                       // shared expert j's piece from token b_row0
+      d1.pad = (d1.a_row0 / I) * Tpad + d1.b_row0;
+    }
+    dm_groups[g] = d1;
   }
 }
 

@@ -8,10 +8,11 @@
 
 // Workspace of the layer backward.  Rall = T·k + Ks·T expert input rows
 // (routed rows, then each shared expert's T rows); P = 2 (SwiGLU) or 1 (ReLU)
-// pre-activation blocks per row.  The K-major weight-gradient operands
-// (g act)ᵀ and dh1ᵀ hold the shared experts' T rows first (each padded to
-// Tpad) and then each routed expert's rows (padded to kSegAlign); KX is the
-// padded extent of one shared block plus all routed segments.
+// pre-activation blocks per row.  The weight-gradient GEMMs' row-major
+// operands g act (gactp) and dh1 (dh1p) sit in a padded row space: each
+// shared expert's T rows padded to Tpad, then each routed expert's rows
+// padded to kSegAlign.  KX is one shared block plus all routed segments, KA
+// every shared block plus the routed segments.
 struct BwdWs {
   float* logits;
   int32_t* idx;
@@ -27,7 +28,8 @@ struct BwdWs {
   __nv_bfloat16 *a, *c, *dm;             // [Rall, I]
   __nv_bfloat16* dh1p;                   // [KA, P·I]: padded row space
   float* row_gate;                       // [Tk]
-  float* dg_part;                        // [Tk, I / 64]: <dm, act> per 64-feature block
+  float* dg_part;                        // [Tk, I / 32]: <dm, act> per feature block
+                                         // (32 features: SwiGLU; 64: ReLU)
   __nv_bfloat16* dz;                     // [T, Epad], zeros past E
   int Epad;                              // E rounded up to 64
   float* du_router;                      // [T, H]
@@ -38,9 +40,28 @@ struct BwdWs {
   int *wp2, *wp13;
   __nv_bfloat16* gactp;                  // [KA, I]: g act, padded row space
   GroupDesc* dxg;                        // the input-gradient GEMM's groups
+  GroupDesc* dmg;                        // the fused dm GEMM's groups (SwiGLU)
+  float* dc_part;                        // [dc_splits, E, H]: d_centroids partial sums
+  int dc_splits, dc_split_blocks;        // contraction ranges of d_centroids, k-chunks each
   long long Tpad, KX, KA;
   size_t total;
 };
+
+// d_centroids = dzᵀ u contracts over all T tokens but has only
+// ceil(Epad / 256) · ceil(H / 256) output tiles: the contraction is cut into
+// ranges so that about one wave of CTA pairs (kDcTiles tiles) is busy, each
+// range's partial sum written apart and the ranges added in order after.
+constexpr int kDcTiles = 72;
+constexpr int kDcMaxSplits = 16;
+
+void dcent_splits(const moe_shape* s, long long Tpad, int Epad, int* splits, int* blocks) {
+  const int tiles = cdiv(Epad, 256) * cdiv(s->H, 256);
+  const int nkb = static_cast<int>(Tpad / tc::kBK);
+  int want = std::max(1, std::min({kDcMaxSplits, kDcTiles / tiles, nkb / tc::kKPS}));
+  const int per = cdiv(cdiv(nkb, want), tc::kKPS) * tc::kKPS;
+  *blocks = std::max(per, tc::kKPS);
+  *splits = std::max(1, cdiv(nkb, *blocks));
+}
 
 BwdWs carve_bwd(void* ws, const moe_shape* s) {
   const size_t T = s->T, E = s->n_routed, k = s->top_k, Ks = s->n_shared, H = s->H,
@@ -79,10 +100,10 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.d_perm = bf(Tk * H);
   B.a = bf(Rall * I);
   B.c = P == 2 ? bf(Rall * I) : nullptr;
-  B.dm = bf(Rall * I);
+  B.dm = P == 2 ? nullptr : bf(Rall * I);   // SwiGLU: dm stays in the GEMM's accumulator
 
   B.row_gate = static_cast<float*>(take(Tk * 4));
-  B.dg_part = static_cast<float*>(take(Tk * (I / 64) * 4));
+  B.dg_part = static_cast<float*>(take(Tk * (I / 32) * 4));
   B.Epad = static_cast<int>((E + tc::kBK - 1) / tc::kBK * tc::kBK);
   B.dz = bf(T * static_cast<size_t>(B.Epad));
   B.du_router = static_cast<float*>(take(T * H * 4));
@@ -99,6 +120,9 @@ BwdWs carve_bwd(void* ws, const moe_shape* s) {
   B.dh1p = bf(P * I * static_cast<size_t>(B.KA));
   B.gactp = bf(I * static_cast<size_t>(B.KA));
   B.dxg = static_cast<GroupDesc*>(take(G * sizeof(GroupDesc)));
+  B.dmg = static_cast<GroupDesc*>(take(G * sizeof(GroupDesc)));
+  dcent_splits(s, B.Tpad, B.Epad, &B.dc_splits, &B.dc_split_blocks);
+  B.dc_part = static_cast<float*>(take(static_cast<size_t>(B.dc_splits) * E * H * 4));
   B.total = off;
   return B;
 }
@@ -195,7 +219,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   const int nt2 = cdiv(H, 256), nt13 = cdiv(I, 256);
   wgrad_plan_kernel<<<1, 1024, 0, st>>>(B.offsets, E, Ks, static_cast<int>(B.Tpad), H, I, P,
                                         B.seg_start, B.wg2, B.wk2, B.wg13, B.wk13, nt2, nt13,
-                                        B.wp2, B.wp13, B.g2, G, Tk, T, B.dxg);
+                                        B.wp2, B.wp13, B.g2, G, Tk, T, B.dxg, B.g1, B.dmg);
   MOE_CUDA(cudaGetLastError());
   const int rmax = static_cast<int>(B.KX - B.Tpad);
   const long long tpad = B.Tpad, sh = static_cast<long long>(Ks) * B.Tpad;
@@ -246,22 +270,51 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     if (swiglu)
       MOE_TRY(row_gemm(wt->w3, wt->sw3, I, H, false, xr, u, T, B.g1, B.c, Rall, B.c, Rall, I));
   }
+  if (swiglu) {
+    // dm = dh W2 (W2 [H, I] per expert is the operand's transpose, read
+    // MN-major) with the SwiGLU derivative in the epilogue: da | dc into
+    // dh1p, g act into gactp (padded row space, zero padding rows), <dm, act>
+    // per routed row and 32-feature block into dg_part; a and c come in by TMA
+    tc::Params p;
+    memset(&p, 0, sizeof(p));
+    MOE_TRY(make_map3_mn(&p.a[0], wt->w2, static_cast<uint64_t>(E) * H, I));
+    if (Ks) MOE_TRY(make_map3_mn(&p.a[1], wt->sw2, static_cast<uint64_t>(Ks) * H, I));
+    else p.a[1] = p.a[0];
+    p.a_mn = 1;
+    p.a_mn_per_expert = I;
+    p.a_k_per_expert = H;
+    MOE_TRY(make_token_maps(p.b[1], dh, T, H));
+    if (dr != nullptr) MOE_TRY(make_token_maps(p.b[0], dr, Tk, H));
+    else memcpy(p.b[0], p.b[1], sizeof(p.b[0]));
+    p.groups = B.dmg;
+    p.tile_prefix = B.tile_prefix;
+    p.n_groups = G;
+    p.n_wtiles = cdiv(I, tc::kBM * pair);
+    p.num_k_blocks = cdiv(H, tc::kBK);
+    p.out_cols = I;
+    p.out_ld = I;
+    p.out[0] = B.dh1p;
+    p.out[1] = B.gactp;
+    // a and c in boxes of 32 columns x 32 rows (the bf16 output-map shape)
+    MOE_TRY(make_out_map(&p.bwd_map[0], B.a, static_cast<uint64_t>(Rall), I));
+    MOE_TRY(make_out_map(&p.bwd_map[1], B.c, static_cast<uint64_t>(Rall), I));
+    p.bwd_gate = B.row_gate;
+    p.bwd_dg = B.dg_part;
+    p.bwd_routed_rows = Tk;
+    p.pad_rows = kSegAlign;
+    MOE_TRY(launch_ffn<tc::EPI_SWIGLU_BWD>(p, bn, st));
+  } else {
   // dm = dh W2: W2 [H, I] per expert is the operand's transpose
   MOE_TRY(row_gemm(wt->w2, wt->sw2, I, H, true, dr, dh, T, B.g1, B.dm, Rall, B.dm, Rall, I));
 
-  // ---- activation derivative (row-major and K-major), gate-scaled
-  // activation (K-major), <dm, act> per routed row and 64-feature block
+  // ---- ReLU derivative and gate-scaled activation into the padded row
+  // space, <dm, act> per routed row and 64-feature block
   {
     auto act_bwd = [&](dim3 grid, long long row_base, int rows_total, const int32_t* seg,
                        long long col0) -> moe_status {
-      if (swiglu)
-        act_backward_kernel<true><<<grid, 256, 0, st>>>(
-            B.a, B.c, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
-            B.dh1p, B.gactp, col0, B.dg_part);
-      else
-        act_backward_kernel<false><<<grid, 256, 0, st>>>(
-            B.a, nullptr, B.dm, B.row_gate, Tk, I, row_base, rows_total, seg, B.offsets, E,
-            B.dh1p, B.gactp, col0, B.dg_part);
+      relu_backward_kernel<<<grid, 256, 0, st>>>(B.a, B.dm, B.row_gate, Tk, I, row_base,
+                                                 rows_total, seg, B.offsets, E, B.dh1p,
+                                                 B.gactp, col0, B.dg_part);
       MOE_CUDA(cudaGetLastError());
       return MOE_OK;
     };
@@ -271,6 +324,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     if (Tk > 0)
       MOE_TRY(act_bwd(dim3(static_cast<unsigned>(cdiv(rmax, 64)), I / 64), 0, 0, B.seg_start, sh));
   }
+  }  // ReLU
 
   }  // Rall > 0
   // ---- gate gradient and the router's share of du and of the centroids
@@ -280,7 +334,8 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     const int gate = s->gate == MOE_GATE_SOFTMAX ? 0 : 1;
 #define MOE_GATE_BWD(N)                                                                 \
   gate_backward_kernel<N><<<blocks, 256, 0, st>>>(B.logits, B.idx, B.w, B.slot_row, B.dg_part, \
-                                                  I / 64, T, E, k, gate, Epad, B.dz)
+                                                  swiglu ? I / 32 : I / 64, T, E, k, gate,  \
+                                                  Epad, B.dz)
     if (npl <= 1) MOE_GATE_BWD(1);
     else if (npl <= 2) MOE_GATE_BWD(2);
     else if (npl <= 4) MOE_GATE_BWD(4);
@@ -326,11 +381,23 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     q.dense_count = H;
     q.n_wtiles = cdiv(Epad, 256);
     q.num_k_blocks = static_cast<int>(B.Tpad / tc::kBK);
-    q.out[0] = q.out[1] = gr->d_centroids;
+    q.k_splits = B.dc_splits;
+    q.k_split_blocks = B.dc_split_blocks;
+    q.split_stride = static_cast<long long>(E) * H;
+    q.out[0] = q.out[1] = B.dc_part;
     q.out_ld = H;
     q.out_cols = E;
     q.out_tr = 1;
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(q, INT_MAX, st)));
+    // the ranges' partial sums, added in range order
+    const long long n4 = static_cast<long long>(E) * H / 4;
+    const int sp_blocks = static_cast<int>(
+        std::min<long long>(one_wave_blocks(sum_partials_kernel, 256), (n4 + 255) / 256));
+    if (sp_blocks <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+    sum_partials_kernel<<<sp_blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(B.dc_part),
+                                                   B.dc_splits, n4,
+                                                   reinterpret_cast<float4*>(gr->d_centroids));
+    MOE_CUDA(cudaGetLastError());
   }
 
   // ---- dx = dh1 [W1; W3] per expert row, then du
@@ -384,7 +451,27 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   MOE_CUDA(cudaGetLastError());
 
   // ---- weight gradients: contractions over each expert's own rows; the
-  // row-major operands (dh and x rows) are read MN-major where they are
+  // row-major operands (dh and x rows) are read MN-major where they are.
+  // The shared experts' groups come first and contract over Tpad rows, the
+  // routed ones over about T·k/E: the two-class tile order (long tiles
+  // dealt first, the clusters that drew one more of them taking fewer of the
+  // rest) keeps every cluster's work about even.
+  auto wgrad_order = [&](tc::Params& p, int tiles_per_group, int long_groups) -> moe_status {
+    if (long_groups == 0) return MOE_OK;
+    int grid = 0;
+    MOE_TRY((tc_grid<tc::EPI_F32, 256, 2>(&grid)));
+    const int clusters = std::max(1, grid / 2);
+    const int nh = long_groups * tiles_per_group;
+    const int nl = (p.n_groups - long_groups) * tiles_per_group;
+    const int r = nh % clusters;
+    // a tile's cost in k-chunks, plus about four for its epilogue
+    const double c_long = static_cast<double>(B.Tpad) / tc::kBK + 4.0;
+    const double c_short = (E > 0 ? static_cast<double>(Tk) / E : 0.0) / tc::kBK + 1.0 + 4.0;
+    const int D = r ? static_cast<int>(std::lround(c_long / c_short)) : 0;
+    p.sched_heavy = nh;
+    p.sched_qb = std::max(0, cdiv(std::max(0, nl - D * (clusters - r)), clusters));
+    return MOE_OK;
+  };
   {  // dW2[e][h][i] = Σ_r dh_r[h] · (g act)_r[i]
     tc::Params p;
     memset(&p, 0, sizeof(p));
@@ -412,6 +499,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     MOE_TRY(make_out_map_f32(&p.omap32[0], p.out[0], static_cast<uint64_t>(E) * H, I));
     MOE_TRY(make_out_map_f32(&p.omap32[1], p.out[1],
                              static_cast<uint64_t>(Ks ? Ks : E) * H, I));
+    MOE_TRY(wgrad_order(p, p.n_wtiles * nt2, Ks));
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
   }
   {  // dW1[e][i][h] = Σ_r da_r[i] · x_r[h], dW3 likewise with dc
@@ -445,6 +533,7 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
       MOE_TRY(make_out_map_f32(&p.omap32[o], p.out[o],
                                static_cast<uint64_t>(sh ? Ks : E) * I, H));
     }
+    MOE_TRY(wgrad_order(p, p.n_wtiles * nt13, Ks * P));
     MOE_TRY((launch_tc<tc::EPI_F32, 256, 2>(p, INT_MAX, st)));
   }
   return MOE_OK;

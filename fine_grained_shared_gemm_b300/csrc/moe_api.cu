@@ -210,21 +210,14 @@ moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, u
 }
 
 
-// Launches the grouped GEMM persistently: one CTA per SM, or for PAIR == 2
-// as many two-CTA clusters as fit on the device at once (at most max_ctas
-// CTAs).  The dynamic shared-memory limit and the grid are set up once per
-// device.
+// The persistent grid of the grouped GEMM: one CTA per SM, or for PAIR == 2
+// as many two-CTA clusters as fit on the device at once.  The dynamic
+// shared-memory limit and the grid are set up once per device.
 template <int EPI, int BN, int PAIR>
-moe_status launch_tc(const tc::Params& p, int max_ctas, cudaStream_t st) {
+cudaLaunchConfig_t tc_config(cudaLaunchAttribute* attr, cudaStream_t st) {
   using C = tc::Config<BN, PAIR>;
-  auto kern = tc::grouped_gemm_kernel<EPI, BN, PAIR>;
-  static int grid_for[64] = {0};
-  int dev = 0;
-  MOE_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
   attr[0].val.clusterDim.y = 1;
@@ -234,11 +227,24 @@ moe_status launch_tc(const tc::Params& p, int max_ctas, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR == 2 ? 1 : 0;
+  return cfg;
+}
+
+template <int EPI, int BN, int PAIR>
+moe_status tc_grid(int* grid) {
+  using C = tc::Config<BN, PAIR>;
+  auto kern = tc::grouped_gemm_kernel<EPI, BN, PAIR>;
+  static int grid_for[64] = {0};
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
   if (grid_for[dev] == 0) {
     MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   C::kSmemBytes));
     int g = num_sms();
     if (PAIR == 2) {
+      cudaLaunchAttribute attr[1];
+      cudaLaunchConfig_t cfg = tc_config<EPI, BN, PAIR>(attr, nullptr);
       int clusters = 0;
       cfg.gridDim = dim3(static_cast<unsigned>(g - g % 2), 1, 1);
       MOE_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
@@ -247,10 +253,21 @@ moe_status launch_tc(const tc::Params& p, int max_ctas, cudaStream_t st) {
     }
     grid_for[dev] = g;
   }
-  int grid = std::min(grid_for[dev], std::max(max_ctas, PAIR));
+  *grid = grid_for[dev];
+  return MOE_OK;
+}
+
+// Launches the grouped GEMM persistently on its grid (at most max_ctas CTAs).
+template <int EPI, int BN, int PAIR>
+moe_status launch_tc(const tc::Params& p, int max_ctas, cudaStream_t st) {
+  int grid = 0;
+  MOE_TRY((tc_grid<EPI, BN, PAIR>(&grid)));
+  grid = std::min(grid, std::max(max_ctas, PAIR));
   grid -= grid % PAIR;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = tc_config<EPI, BN, PAIR>(attr, st);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  MOE_CUDA(cudaLaunchKernelEx(&cfg, kern, p));
+  MOE_CUDA(cudaLaunchKernelEx(&cfg, tc::grouped_gemm_kernel<EPI, BN, PAIR>, p));
   return MOE_OK;
 }
 

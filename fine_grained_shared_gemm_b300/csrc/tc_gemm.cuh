@@ -73,12 +73,14 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
 // Epilogue scratch per epilogue warp: two 2 KB staging tiles for bulk
 // stores (32 x 32 bf16, or one 32 x 32 fp32 tile over both) and the SwiGLU
-// hand-off area (16 x 33 floats).
-constexpr int kEpiWarpBytes = 6272;
+// hand-off area (16 x 33 floats); or, for the SwiGLU derivative, a chunk's
+// a and c tiles (4 KB) and three 16-row output tiles (3 KB).  With 7 KB a
+// warp the 256-token pair tile still keeps three pipeline stages.
+constexpr int kEpiWarpBytes = 7168;
 constexpr int kHandoffOffset = 4096;
 constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 family
 
-enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3 };
+enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3, EPI_SWIGLU_BWD = 4 };
 
 struct Params {
   CUtensorMap a[2];              // weight stacks (routed, shared): 3-D, or 5-D for SwiGLU
@@ -102,9 +104,11 @@ struct Params {
   // Token operand MN-major (b_mn): the token side is read in its stored
   // row-major layout as the transpose of the operand — operand element
   // (n, k) at row k, column n — through maps (64 columns, rows, column
-  // blocks of 64) with a box of 64 columns x kKPS·64 rows x 2 blocks; every
-  // tile is BN columns wide (columns past the matrix are zero-filled, only
-  // the valid ones are stored).  b_k_rows: k starts at row krange.y.
+  // blocks of 64) with a box of 64 columns x kKPS·64 rows x 2 blocks; a tile
+  // is BN columns wide, or BN / 2 when it holds at most that many valid
+  // columns and each CTA's half is still whole 64-column blocks (columns
+  // past the matrix are zero-filled, only the valid ones are stored).
+  // b_k_rows: k starts at row krange.y.
   int b_mn;
   int b_k_rows;
   CUtensorMap b[2][kNumBoxes];   // token sources x box heights: 3-D
@@ -120,6 +124,23 @@ struct Params {
   // of kKPS; 0 makes the tile's output zeros).  Used by the weight-gradient
   // GEMMs, whose contraction runs over each expert's own token rows.
   const int4* krange;
+  // Dense group only (no krange): the contraction is cut into k_splits
+  // ranges of k_split_blocks k-chunks (a multiple of kKPS; the last range
+  // takes the rest).  Tile t computes range t / (n_wtiles · token tiles)
+  // and writes it split_stride elements after the previous range's output
+  // (plain or transposed fp32 stores, no f32_tma): partial sums that a
+  // later pass adds in range order.
+  int k_splits;
+  int k_split_blocks;
+  long long split_stride;
+  // Tile order.  sched_heavy == 0: every cluster (CTA pair, or CTA) c of P
+  // takes tiles c, c + P, c + 2P, ...  sched_heavy = nh > 0: tiles [0, nh)
+  // are long ones (contractions several times the rest's), dealt round
+  // robin first; the other tiles follow round robin too, but the nh mod P
+  // clusters that drew one more long tile stop after sched_qb rounds while
+  // the others go on, so every cluster ends with about the same work.
+  int sched_heavy;
+  int sched_qb;
   void* out[4];
   int out_ld;                    // output row pitch in elements
   int out_cols;                  // valid output columns
@@ -137,6 +158,25 @@ struct Params {
   int save;
   void* save_out[2];
   CUtensorMap save_map[2];
+  // EPI_SWIGLU_BWD: the accumulator is dm = dh W2 for the tile's rows (the
+  // output row space of the groups: out_row0 = the rows' index into the
+  // pre-activations a, c [rows, out_cols], read through bwd_map[0] and
+  // bwd_map[1], boxes of 32 columns x 32 rows; routed rows
+  // [0, bwd_routed_rows) first).  Per row r and feature f, with g the routed
+  // row's gate weight (1 for a shared row) and act = SiLU(a) ⊙ c:
+  //   out[0] (dh1, [padded rows, 2·out_cols]):  da = g dm ⊙ c ⊙ SiLU'(a)
+  //     at column f, dc = g dm ⊙ SiLU(a) at column out_cols + f;
+  //   out[1] (g act, [padded rows, out_cols]):  g act at column f;
+  //   bwd_dg[r · (out_cols / 32) + f / 32] = Σ over f's 32-feature block of
+  //     dm ⊙ act (routed rows only).
+  // The outputs sit in a padded row space: a group's rows start at its
+  // GroupDesc.pad, and its rows past count up to the next multiple of
+  // pad_rows are written as zeros.
+  CUtensorMap bwd_map[2];
+  const float* bwd_gate;
+  float* bwd_dg;
+  int bwd_routed_rows;
+  int pad_rows;
 };
 
 constexpr int kMaxGroups = 1024;
@@ -288,6 +328,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
+}
+
+// A 2-D box pulled into L2 ahead of its load.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// A 2-D box into this CTA's own shared memory, completion on its own barrier.
+__device__ __forceinline__ void tma_load_2d_local(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
 }
 
 template <int PAIR>
@@ -556,6 +614,9 @@ struct Tile {
   int n_valid;           // valid token rows of the tile
   int nt;                // token tiles of the tile's group
   int ka0, kb0, nk;      // first k-chunk of each operand, k-chunks
+  int split;             // contraction range of a dense split-K launch
+  int prow;              // EPI_SWIGLU_BWD: the tile's first row in the padded row space
+  int pad_end;           // EPI_SWIGLU_BWD: rows written (valid, then zero padding)
 };
 
 // Group of tile t (0 for a dense group).
@@ -575,11 +636,15 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   constexpr int kStep = Config<BN, PAIR>::kStep;
   const int nw = p.n_wtiles;
   GroupDesc d;
-  int nt, local, lo = 0;
+  int nt, local, lo = 0, split = 0;
   if (p.groups == nullptr) {
     d = GroupDesc{0, 0, 0, 0, 0, 0, p.dense_count, 0};
     nt = (p.dense_count + BN - 1) / BN;
     local = t;
+    if (p.k_splits > 1) {
+      split = t / (nw * nt);
+      local = t - split * (nw * nt);
+    }
   } else {
     int hi = p.n_groups;  // largest g with prefix[g] * nw <= t
     while (hi - lo > 1) {
@@ -600,7 +665,9 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.n_valid = min(th, d.count - n * th);
   tl.n_mma = (tl.n_valid + kStep - 1) / kStep * kStep;
   tl.nt = nt;
-  if (p.b_mn) tl.n_mma = BN;  // MN-major tokens: whole 64-column blocks per CTA
+  // MN-major tokens: whole 64-column blocks per CTA
+  constexpr bool kHalfMN = (BN / 2 / PAIR) % 64 == 0;
+  if (p.b_mn) tl.n_mma = (kHalfMN && tl.n_valid <= BN / 2) ? BN / 2 : BN;
   tl.b_rows = tl.n_mma / PAIR;
   tl.b_box = box_index(tl.b_rows);
   tl.b_src = d.b_src;
@@ -608,16 +675,42 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.out_sel = d.out_sel;
   tl.out_row = d.out_row0 + n * th;
   tl.out_col = (w * PAIR + rank) * kCols;
+  tl.split = split;
+  if (EPI == EPI_SWIGLU_BWD) {
+    tl.prow = d.pad + n * th;
+    tl.pad_end = n == nt - 1 ? (d.count + p.pad_rows - 1) / p.pad_rows * p.pad_rows - n * th : th;
+  }
   if (p.krange != nullptr) {
     const int4 kr = __ldg(p.krange + lo);
     tl.ka0 = kr.x;
     tl.kb0 = kr.y;
     tl.nk = kr.z;
+  } else if (p.k_splits > 1) {
+    tl.ka0 = tl.kb0 = split * p.k_split_blocks;
+    tl.nk = max(0, min(p.k_split_blocks, p.num_k_blocks - tl.ka0));
   } else {
     tl.ka0 = tl.kb0 = 0;
     tl.nk = p.num_k_blocks;
   }
   return tl;
+}
+
+// Tile of iteration i of cluster c of P (Params.sched_heavy), or -1 past the
+// cluster's last.  Every role of both CTAs walks the same sequence.
+__device__ __forceinline__ int sched_tile(const Params& p, int c, int P, int total, int i) {
+  if (p.sched_heavy <= 0) {
+    const int t = c + i * P;
+    return t < total ? t : -1;
+  }
+  const int nh = p.sched_heavy;
+  const int hc = nh > c ? (nh - 1 - c) / P + 1 : 0;  // long tiles c, c + P, ...
+  if (i < hc) return c + i * P;
+  const int k = i - hc, r = nh % P, qb = p.sched_qb;
+  int idx;                                            // among the other tiles
+  if (k < qb) idx = k * P + c;                        // rounds every cluster takes
+  else if (c < r) return -1;                          // drew one more long tile
+  else idx = qb * P + (k - qb) * (P - r) + (c - r);   // rounds of the other P - r
+  return idx < total - nh ? nh + idx : -1;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -637,6 +730,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 256u + 8u * a; };
   auto tempty_bar = [&](int a) { return bar0 + 272u + 8u * a; };
   const uint32_t done_bar = bar0 + 288u;
+  // EPI_SWIGLU_BWD: each epilogue warp's input-tile barrier
+  auto ld_bar = [&](int q) { return bar0 + 320u + 8u * q; };
   uint8_t* bar_area = smem + S * C::kStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 296);
   int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
@@ -657,6 +752,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(tempty_bar(a), 4 * PAIR);  // lane 0 of each epilogue warp of each CTA
     }
     mbar_init(done_bar, 1);
+    if (EPI == EPI_SWIGLU_BWD)
+      for (int q = 0; q < 4; ++q) mbar_init(ld_bar(q), 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -675,7 +772,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int tiles_per_w = (p.groups == nullptr) ? (p.dense_count + BN - 1) / BN
                                                 : s_prefix[p.n_groups];
-  const int total = p.n_wtiles * tiles_per_w;
+  const int total = p.n_wtiles * tiles_per_w * (p.k_splits > 1 ? p.k_splits : 1);
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -687,7 +784,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // through (evict first); one that several token tiles read, and the
       // token rows (read by every weight tile of their group), stay (evict last)
       const uint64_t pol_once = l2_policy_evict_first(), pol_keep = l2_policy_evict_last();
-      for (int t = first; t < total && ok; t += stride) {
+      for (int i = 0; ok; ++i) {
+        const int t = sched_tile(p, first, stride, total, i);
+        if (t < 0) break;
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
         const uint64_t pol_a = tl.nt > 1 ? pol_keep : pol_once;
         // token rows each CTA's copy lands per k-block (MN-major: BN / PAIR
@@ -760,7 +859,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int stage = 0, a0 = 0;
       uint32_t phase = 0, acc_ph[2] = {0u, 0u};
       bool ok = true;
-      for (int t = first; t < total && ok; t += stride) {
+      for (int i = 0; ok; ++i) {
+        const int t = sched_tile(p, first, stride, total, i);
+        if (t < 0) break;
         const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, 0);
         if (!mbar_wait<PAIR == 2>(tempty_bar(a0), acc_ph[a0] ^ 1)) {
           raise_device_error(DEV_ERR_TIMEOUT_MMA);
@@ -827,6 +928,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     int a0 = 0;
     uint32_t acc_ph[2] = {0u, 0u};
     uint32_t n_stores = 0;  // bulk stores this warp has issued (selects the staging buffer)
+    // EPI_SWIGLU_BWD: the a and c tiles of one chunk land in this warp's
+    // staging area (a at [0, 2 KB), c at [2 KB, 4 KB)) on ld_bar(q); 16 rows
+    // of the three outputs are staged at [4 KB, 7 KB) for 16-byte stores;
+    // lane L holds the gate weight of row L of the next chunk
+    uint16_t* ostg = reinterpret_cast<uint16_t*>(buf) + 2048;
+    float gate_next = 1.0f;
+    auto load_gate = [&](const Tile& tl, int c0) {
+      const long long r = static_cast<long long>(tl.out_row) + c0 + lane;
+      gate_next = (c0 + lane < tl.n_valid && r < p.bwd_routed_rows) ? __ldg(p.bwd_gate + r) : 1.0f;
+    };
+    uint32_t ld_ph = 0;
+    bool ld_pending = false, ld_failed = false;
+    auto load_inputs = [&](int col, int row) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(ld_bar(q), 4096u);
+        tma_load_2d_local(smem_u32(buf), &p.bwd_map[0], ld_bar(q), col, row);
+        tma_load_2d_local(smem_u32(buf) + 2048u, &p.bwd_map[1], ld_bar(q), col, row);
+      }
+      ld_pending = true;
+    };
     // this warp has read accumulator slot a: tell the leader's MMA issuer
     auto release = [&](int a) {
       tc_fence_before();
@@ -837,8 +958,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       acc_ph[a] ^= 1u;
     };
-    for (int t = first; t < total; t += stride) {
+    for (int i = 0;; ++i) {
+      const int t = sched_tile(p, first, stride, total, i);
+      if (t < 0) break;
       const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
+      // the first chunk's inputs are on their way while the MMAs run
+      const bool bwd_active = EPI == EPI_SWIGLU_BWD && !ld_failed &&
+                              tl.out_col + q * 32 < p.out_cols && tl.n_valid > 0;
+      if (bwd_active) {
+        const int f0 = tl.out_col + q * 32;
+        if (lane == 0)   // every chunk's a and c boxes into L2
+          for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+            tma_prefetch_2d(&p.bwd_map[0], f0, tl.out_row + c0);
+            tma_prefetch_2d(&p.bwd_map[1], f0, tl.out_row + c0);
+          }
+        load_inputs(f0, tl.out_row);
+        load_gate(tl, 0);
+      }
       const bool ready = mbar_wait(tfull_bar(a0), acc_ph[a0]);
       // all four epilogue warps leave together, so no named barrier is left half-arrived
       if (!named_bar_and(1, 128, ready)) {
@@ -958,7 +1094,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               (p.col_offset != nullptr && col_ok) ? __ldg(p.col_offset + col) : 0.0f;
           if (col_ok && p.out_tr) {
             // transposed: this lane's 32 token rows are 32 consecutive floats
-            float* o = static_cast<float*>(p.out[tl.out_sel]) +
+            float* o = static_cast<float*>(p.out[tl.out_sel]) + tl.split * p.split_stride +
                        static_cast<size_t>(col) * p.out_ld + tl.out_row + c0;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -981,7 +1117,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               bulk_commit();
             }
           } else if (col_ok) {
-            float* o = static_cast<float*>(p.out[tl.out_sel]) +
+            float* o = static_cast<float*>(p.out[tl.out_sel]) + tl.split * p.split_stride +
                        static_cast<size_t>(tl.out_row + c0) * p.out_ld + col;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -999,12 +1135,112 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     q * 32);
         }
       };
-      // column c of the slot holds token row c of the tile (one call site
-      // keeps the chunk body inlined once)
-      for (int c0 = 0; c0 < tl.n_valid; c0 += 32) chunk(a0 * BN + c0, c0);
+      if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // This lane's feature f0 + lane, 32 token rows per chunk: dm from
+        // the accumulator, a and c from the chunk's input tiles (the next
+        // chunk's are requested as soon as these are read), da / dc / g act
+        // staged 16 rows at a time and stored as 16-byte vectors, <dm, act>
+        // summed over the warp's 32 features.  Chunks past the tile's valid
+        // rows (its group's padding) are zeros.
+        const int f0 = tl.out_col + q * 32;
+        if (bwd_active) {
+          const int nf = p.out_cols;
+          const uint16_t* in = reinterpret_cast<const uint16_t*>(buf);
+          for (int c0 = 0; c0 < tl.pad_end; c0 += 32) {
+            const int nrow = max(0, min(32, tl.n_valid - c0));
+            const long long r0 = static_cast<long long>(tl.out_row) + c0;
+            float av[32], cv[32], dm[32];
+            const float g_lane = gate_next;
+            load_gate(tl, c0 + 32);  // the next chunk's, in flight during this one
+            uint32_t v[32];
+            if (nrow > 0) tmem_ld32(tlane + static_cast<uint32_t>(a0 * BN + c0), v);
+            if (nrow > 0 && !ld_failed) {
+              if (!mbar_wait(ld_bar(q), ld_ph)) {
+                raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
+                ld_failed = true;
+              } else {
+                ld_ph ^= 1u;
+                ld_pending = false;
+              }
+            }
+            if (nrow > 0 && !ld_failed) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                av[j] = j < nrow ? __bfloat162float(__ushort_as_bfloat16(in[j * 32 + lane])) : 0.0f;
+                cv[j] = j < nrow ? __bfloat162float(__ushort_as_bfloat16(in[1024 + j * 32 + lane]))
+                                 : 0.0f;
+              }
+              // every lane's reads of the tiles are ordered before the async
+              // proxy refills them
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (c0 + 32 < tl.n_valid) load_inputs(f0, tl.out_row + c0 + 32);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) dm[j] = j < nrow ? __uint_as_float(v[j]) : 0.0f;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) av[j] = cv[j] = dm[j] = 0.0f;
+            }
+            // 16 rows at a time: the three outputs into the staging tiles,
+            // then out as 16-byte vectors (4 lanes per 64-byte row segment)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const int j = h * 16 + jj;
+                const float g = __shfl_sync(0xffffffffu, g_lane, j);
+                // sigmoid(a) = (1 + tanh(a / 2)) / 2, as in the forward's SiLU
+                const float sg = fmaf(0.5f, tanh_approx(0.5f * av[j]), 0.5f);
+                const float si = av[j] * sg;
+                const float act = si * cv[j];
+                const float gd = g * dm[j];
+                ostg[jj * 32 + lane] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(gd * cv[j] * sg * (1.0f + av[j] * (1.0f - sg))));
+                ostg[512 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(gd * si));
+                ostg[1024 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(g * act));
+                dm[j] *= act;  // this lane's share of <dm, act> for row j
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 6; ++i) {
+                const int vi = i * 32 + lane;        // 16-byte vector: output, row, 8 columns
+                const int o = vi >> 6, row = (vi >> 2) & 15, c8 = (vi & 3) * 8;
+                const uint4 val = *reinterpret_cast<const uint4*>(ostg + o * 512 + row * 32 + c8);
+                // outputs 0, 1: dh1's da and dc halves (pitch 2·nf); 2: g act
+                __nv_bfloat16* const base =
+                    static_cast<__nv_bfloat16*>(o < 2 ? p.out[0] : p.out[1]) + (o == 1 ? nf : 0);
+                const size_t pitch = o < 2 ? 2 * static_cast<size_t>(nf) : static_cast<size_t>(nf);
+                *reinterpret_cast<uint4*>(
+                    base + static_cast<size_t>(tl.prow + c0 + h * 16 + row) * pitch + f0 + c8) = val;
+              }
+              __syncwarp();  // the staging tiles are read before the next rows fill them
+            }
+            // sum over the 32 lanes, scattered so that lane j ends with row j
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) {
+              const bool up = (lane & sh) != 0;
+#pragma unroll
+              for (int i2 = 0; i2 < sh; ++i2) {
+                const float send = up ? dm[i2] : dm[i2 + sh];
+                const float keep = up ? dm[i2 + sh] : dm[i2];
+                dm[i2] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
+              }
+            }
+            if (lane < nrow && r0 + lane < p.bwd_routed_rows)
+              p.bwd_dg[static_cast<size_t>(r0 + lane) * (nf / 32) + f0 / 32] = dm[0];
+          }
+        }
+      } else {
+        // column c of the slot holds token row c of the tile (one call site
+        // keeps the chunk body inlined once)
+        for (int c0 = 0; c0 < tl.n_valid; c0 += 32) chunk(a0 * BN + c0, c0);
+      }
       release(a0);
       a0 ^= 1;
     }
+    // no input tile may land after the CTA exits
+    if (EPI == EPI_SWIGLU_BWD && ld_pending && !mbar_wait(ld_bar(q), ld_ph))
+      raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
     if (lane == 0) bulk_wait_all();  // every bulk store has completed before the CTA exits
     __syncwarp();
   }

@@ -63,16 +63,22 @@ def test_decode_roofline_counts_bytes_over_the_layer_time():
 def test_backward_launch_counts():
     s = W.SHAPES["dsmoe16b_bf16"]          # SwiGLU, 2 shared, top-6
     # recompute: logits, route, 4 dispatch, 2 pre-activation GEMMs, then the
-    # common 15: scatter dh rows, row gate, 2 plans, dm, 3 derivative launches
-    # (2 shared + routed), gate, 2 router GEMMs, dx, du, 2 weight-gradient GEMMs
-    assert bench.backward_launches(s, saved=True) == 15
-    assert bench.backward_launches(s) == 15 + 6 + 2
+    # common 13: scatter dh rows, row gate, 2 plans, dm with the SwiGLU
+    # derivative, gate, 2 router GEMMs, the router gradient's partial sums,
+    # dx, du, 2 weight-gradient GEMMs
+    assert bench.backward_launches(s, saved=True) == 13
+    assert bench.backward_launches(s) == 13 + 6 + 2
     relu = W.MoEShape("r", T=64, H=128, n_routed=8, n_shared=0, top_k=0, inter=128,
                       act=W.ACT_RELU)
     # no expert rows at all: no row scatter, dm, derivative or dx; dispatch
     # is one scan when recomputing
-    assert bench.backward_launches(relu, saved=True) == 2 + 3 + 1 + 2
-    assert bench.backward_launches(relu) == 2 + 3 + 1 + 2 + 3
+    assert bench.backward_launches(relu, saved=True) == 2 + 4 + 1 + 2
+    assert bench.backward_launches(relu) == 2 + 4 + 1 + 2 + 3
+    # ReLU with rows: the derivative is its own launch per shared expert and
+    # one for the routed rows
+    relu_rows = W.MoEShape("rr", T=64, H=128, n_routed=8, n_shared=1, top_k=2, inter=128,
+                           act=W.ACT_RELU)
+    assert bench.backward_launches(relu_rows, saved=True) == 2 + 2 + 1 + 2 + 4 + 2 + 2
     assert bench.forward_launches(s) == 10 and bench.forward_launches(relu) == 7
 
 

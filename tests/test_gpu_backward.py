@@ -230,6 +230,45 @@ def test_training_forward_matches_forward(shape):
     assert torch.equal(h, h_train)
 
 
+@pytest.mark.parametrize("shape", [SHAPES[2], SHAPES[3]], ids=lambda s: s.name)
+def test_training_step_replays_from_a_cuda_graph(shape):
+    """moe_layer_forward_train and moe_layer_backward make no host
+    synchronisation or allocation: both capture into one CUDA graph, and its
+    replays give the eager calls' h, du and weight gradients bit for bit."""
+    inp = W.make_inputs(shape, DEV, seed=7)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(8)
+    dh = torch.randn((shape.T, shape.H), generator=gen, device=DEV).to(torch.bfloat16)
+    h_ref, saved_ref = forward_train(shape, inp)
+    du_ref, g_ref = run_backward(shape, inp, dh, saved_ref)
+    # fresh buffers, captured once
+    wt = M.weights_struct(inp)
+    ws_f = M.alloc_workspace(M.moe_layer_workspace_size(shape), DEV)
+    ws_b = M.alloc_workspace(M.moe_layer_backward_workspace_size(shape), DEV)
+    saved = M.alloc_workspace(M.moe_layer_saved_size(shape), DEV)
+    h = torch.empty_like(h_ref)
+    du = torch.empty_like(du_ref)
+    g = grads_buffers(shape)
+    grads = M.weight_grads(g["d_centroids"], g["dw1"], g["dw3"], g["dw2"], g["dsw1"], g["dsw3"],
+                           g["dsw2"])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        M.moe_layer_forward_train(shape, wt, inp.u, h, saved, ws_f)
+        M.moe_layer_backward(shape, wt, inp.u, dh, du, grads, ws_b, saved=saved)
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert M.moe_device_status()[0] == M.MOE_OK
+        assert torch.equal(h, h_ref)
+        assert torch.equal(du, du_ref)
+        for key, t in g.items():
+            if t is not None:
+                assert torch.equal(t, g_ref[key]), key
+        h.zero_()
+        du.zero_()
+
+
 def test_autograd_layer_matches_oracle():
     """The torch.autograd wrapper: gradients of sum(h * dh) through a PyTorch
     model equal the oracle's backward for the kernels' own choice."""
