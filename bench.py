@@ -130,13 +130,20 @@ def prefill_roofline(s: W.MoEShape, offsets: np.ndarray, ffn_s: float, peaks: di
     gb = alg_bytes / ffn_s / 1e9
     t_flops = flops / (peaks["bf16_tflops"] * 1e12)
     t_bytes = alg_bytes / (peaks["hbm_gbs"] * 1e9)
-    return {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-            "algorithmic_flop": flops,
+    r = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+         "algorithmic_flop": flops}
+    if peaks.get("bf16_tflops_sustained"):
+        # the same against the rate measured under a seconds-long load at the
+        # power cap, for a call that ran power-capped (see the clocks record)
+        r["peak_sustained"] = peaks["bf16_tflops_sustained"]
+        r["frac_of_sustained"] = round(tf / peaks["bf16_tflops_sustained"], 4)
+    r.update({
             "other_roof": {"bound": "hbm", "achieved": round(gb, 1), "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": round(gb / peaks["hbm_gbs"], 4),
                            "algorithmic_bytes": alg_bytes},
-            "ridge": "memory side" if t_bytes > t_flops else "tensor side"}
+            "ridge": "memory side" if t_bytes > t_flops else "tensor side"})
+    return r
 
 
 def decode_roofline(s: W.MoEShape, offsets: np.ndarray, layer_s: float, ffn_s: float,
@@ -325,6 +332,13 @@ class Layer:
         M.moe_combine(s, i.u, self.y_perm, self.y_shared, self.w, self.slot_row, self.h)
 
 
+def sustained_frac(flops: float, ms: float, peaks: dict):
+    """flops in ms against the bf16 rate measured under a seconds-long load
+    at the power cap (None without that figure)."""
+    p = peaks.get("bf16_tflops_sustained")
+    return round(flops / (ms / 1e3) / 1e12 / p, 4) if p else None
+
+
 def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
     """Kernel launches of one moe_layer_backward call (counted from its host
     code); saved: the call reuses moe_layer_forward_train's tensors."""
@@ -453,6 +467,8 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
     return {"tokens_per_s": round(s.T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
             "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
             "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained_bf16": (round(tf / peaks["bf16_tflops_sustained"], 4)
+                                       if peaks.get("bf16_tflops_sustained") else None),
             "gpu_launches": backward_launches(s) * K,
             "note": "recomputes routing and the gate/up pre-activations from u; "
                     "weight gradients fp32",
@@ -462,6 +478,7 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
                 "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
                 "tokens_per_s": round(s.T / ((f_ms + b_ms) / 1e3), 1),
                 "tflops": round(step_flops / ((f_ms + b_ms) / 1e3) / 1e12, 1),
+                "frac_of_sustained_bf16": sustained_frac(step_flops, f_ms + b_ms, peaks),
                 "clocks": clk_t.summary(),
                 "note": "moe_layer_forward_train + moe_layer_backward on its saved tensors"},
             "training_step_graph": {
@@ -469,6 +486,7 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
                 "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
                 "tokens_per_s": round(s.T / ((gf_ms + gb_ms) / 1e3), 1),
                 "tflops": round(step_flops / ((gf_ms + gb_ms) / 1e3) / 1e12, 1),
+                "frac_of_sustained_bf16": sustained_frac(step_flops, gf_ms + gb_ms, peaks),
                 "clocks": clk_g.summary(),
                 "note": "the same two calls, each captured into a CUDA graph and replayed"}}
 

@@ -2,18 +2,12 @@
 // (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE", §3.1 Eq. 9–11: shared
 // experts, gate-weighted routed experts, residual).  fp32 accumulation in this
 // fixed order and one rounding to the output type, so the result is the same
-// on every run.  A warp per (token, stretch of the row), 16-byte vectors
-// along H.
+// on every run.  One warp per token, 16-byte vectors along H.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
-
-// Work items are (token, 128-vector stretch of its row): finer than a whole
-// row per warp, so a grid of one wave of resident warps divides the work
-// evenly (a warp per row left the last of ~2.3 waves of rows mostly empty).
-constexpr int kCombineVecsPerItem = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(
@@ -26,23 +20,14 @@ __global__ void __launch_bounds__(256) combine_kernel(
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / V;
-  const int per_tok = (nvec + kCombineVecsPerItem - 1) / kCombineVecsPerItem;
-  const long long items = static_cast<long long>(n_tokens) * per_tok;
-  int t_loaded = -1;
-  for (long long it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps) {
-    const int t = static_cast<int>(it / per_tok);
-    const int v0 = static_cast<int>(it % per_tok) * kCombineVecsPerItem;
-    const int v1 = min(nvec, v0 + kCombineVecsPerItem);
-    if (t != t_loaded) {  // slot s's row and weight, broadcast through shared memory
-      __syncwarp();
-      if (lane < k) {     // k <= 32
-        s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
-        s_w[wib][lane] = __ldg(topk_w + static_cast<size_t>(t) * k + lane);
-      }
-      __syncwarp();
-      t_loaded = t;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += warps) {
+    __syncwarp();
+    if (lane < k) {  // k <= 32: slot s's row and weight, broadcast through shared memory
+      s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
+      s_w[wib][lane] = __ldg(topk_w + static_cast<size_t>(t) * k + lane);
     }
-    for (int v = v0 + lane; v < v1; v += 32) {
+    __syncwarp();
+    for (int v = lane; v < nvec; v += 32) {
       float acc[V], y[V];
       Vec16<T>::load(u + static_cast<size_t>(t) * H + v * V, acc);
       for (int j = 0; j < Ks; ++j) {

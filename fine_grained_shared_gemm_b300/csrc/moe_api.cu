@@ -649,9 +649,7 @@ moe_status do_combine(const moe_shape* s, const void* u, const void* y_perm,
   const int T = s->T;
   if (T == 0) return MOE_OK;
   const bool f32 = s->dtype == MOE_DTYPE_F32;
-  const int blocks = f32 ? one_wave_blocks(combine_kernel<float>, 256)
-                         : one_wave_blocks(combine_kernel<__nv_bfloat16>, 256);
-  if (blocks <= 0) return cuda_fail(cudaErrorInvalidConfiguration);
+  const int blocks = route_blocks(T);
   if (f32)
     combine_kernel<float><<<blocks, 256, 0, st>>>(
         static_cast<const float*>(u), static_cast<const float*>(y_perm),

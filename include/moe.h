@@ -31,7 +31,11 @@
  *  - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and returns without synchronising.  Arguments are
  *    checked on the host before anything is launched; a failed check
- *    launches nothing.  Errors are returned, never thrown.
+ *    launches nothing.  Errors are returned, never thrown.  The device-side
+ *    calls (all but moe_layer_forward_host and moe_device_status) can be
+ *    captured into a CUDA graph on a capturing stream once each has run
+ *    outside a capture (the first call on a device sets the kernels'
+ *    shared-memory limits); a replay repeats the call on the same buffers.
  *  - The expert routing never drops a token (no capacity factor; the
  *    page's §4 states that DeepSeekMoE drops none).
  *

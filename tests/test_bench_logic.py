@@ -6,7 +6,7 @@ import pytest
 import bench
 from fine_grained_shared_gemm_b300 import workloads as W
 
-PEAKS = {"hbm_gbs": 6490.8, "bf16_tflops": 1755.6}
+PEAKS = {"hbm_gbs": 6490.8, "bf16_tflops": 1755.6, "bf16_tflops_sustained": 1384.1}
 
 
 def _even_offsets(s):
@@ -39,6 +39,14 @@ def test_prefill_roofline_is_the_tensor_peak(name):
     t_f = bench.expert_flops(s) / (PEAKS["bf16_tflops"] * 1e12)
     t_b = bench.ffn_alg_bytes(s, off) / (PEAKS["hbm_gbs"] * 1e9)
     assert r["ridge"] == ("memory side" if t_b > t_f else "tensor side")
+    # the fraction of the power-capped rate sits beside the burst one
+    if PEAKS.get("bf16_tflops_sustained"):
+        assert r["frac_of_sustained"] == pytest.approx(
+            r["achieved"] / PEAKS["bf16_tflops_sustained"], rel=1e-3)
+        assert r["frac_of_sustained"] > r["frac"]
+    assert bench.sustained_frac(1.3841e12, 1.0, {"bf16_tflops_sustained": 1384.1}) == \
+        pytest.approx(1.0, rel=1e-4)
+    assert bench.sustained_frac(1e12, 1.0, {}) is None
 
 
 def test_decode_roofline_counts_bytes_over_the_layer_time():
