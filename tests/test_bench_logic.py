@@ -32,6 +32,7 @@ def test_prefill_roofline_is_the_tensor_peak(name):
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert r["achieved"] == pytest.approx(bench.expert_flops(s) / 1e-3 / 1e12, rel=1e-3)
     assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["bf16_tflops"], rel=1e-3)
+    assert r["frac_of_nominal"] == pytest.approx(r["achieved"] / 2250.0, rel=1e-3)
     other = r["other_roof"]
     assert other["bound"] == "hbm"
     assert other["algorithmic_bytes"] == bench.ffn_alg_bytes(s, off)
@@ -63,6 +64,7 @@ def test_decode_roofline_counts_bytes_over_the_layer_time():
     assert r["bound"] == "hbm" and r["experts_touched"] == 101
     assert r["achieved"] == pytest.approx(b / 2e-3 / 1e9, rel=1e-3)
     assert r["ffn_only"]["achieved"] == pytest.approx(w / 1.8e-3 / 1e9, rel=1e-3)
+    assert r["frac_of_nominal"] == pytest.approx(r["achieved"] / 8000.0, rel=1e-3)
     assert "note" not in r
     fast = bench.decode_roofline(s, off, 1e-4, 1e-4, PEAKS)   # above the copy rate
     assert fast["frac"] > 1 and "note" in fast
