@@ -1103,6 +1103,82 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* s, const moe_weights*
   return status;
 }
 
+// Batches pipelined across calls' worth of tokens: batch b + 1's copy in
+// (stream `in`) and batch b - 1's copy back (stream `out`) overlap batch b's
+// layer (the caller's stream).  Two device slots of T rows each for u and
+// h; a slot is refilled once the layer two batches back has read it (u) and
+// its copy back has read it (h).
+MOE_API moe_status moe_layer_forward_host_stream(const moe_shape* s, const moe_weights* weights,
+                                                 int n_batches, const void* const* u_host,
+                                                 void* const* h_host, void* u_dev, void* h_dev,
+                                                 void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(s));
+  if (n_batches < 0) return MOE_ERR_INVALID_ARG;
+  if (n_batches > 0 && s->T > 0) {
+    if (u_host == nullptr || h_host == nullptr || !ok_ptr(u_dev) || !ok_ptr(h_dev))
+      return MOE_ERR_INVALID_ARG;
+    for (int b = 0; b < n_batches; ++b)
+      if (u_host[b] == nullptr || h_host[b] == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(check_weights_ffn(s, weights));
+  if (ws == nullptr || !al16(ws) || ws_bytes < carve_layer(nullptr, s).total)
+    return MOE_ERR_WORKSPACE;
+  if (n_batches == 0 || s->T == 0) return MOE_OK;
+  cudaStream_t st = cs(stream);
+  CopyStreams cp;
+  MOE_TRY(copy_streams(&cp));
+  const size_t bytes = static_cast<size_t>(s->T) * s->H * elt_bytes(s);
+  // start, then per slot: copied in, layer done, copied back
+  cudaEvent_t ev[7];
+  int n_ev = 0;
+  moe_status status = MOE_OK;
+  for (int i = 0; i < 7 && status == MOE_OK; ++i) {
+    const cudaError_t e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) status = cuda_fail(e); else n_ev = i + 1;
+  }
+  cudaEvent_t start = ev[0];
+  cudaEvent_t* in_done = ev + 1;
+  cudaEvent_t* layer_done = ev + 3;
+  cudaEvent_t* out_done = ev + 5;
+  // the copy streams first wait for whatever the caller queued before this call
+  if (status == MOE_OK) {
+    cudaError_t e = cudaEventRecord(start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.in, start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.out, start, 0);
+    if (e != cudaSuccess) status = cuda_fail(e);
+  }
+  for (int b = 0; b < n_batches && status == MOE_OK; ++b) {
+    const int slot = b & 1;
+    char* u_slot = static_cast<char*>(u_dev) + slot * bytes;
+    char* h_slot = static_cast<char*>(h_dev) + slot * bytes;
+    cudaError_t e = cudaSuccess;
+    if (b >= 2) e = cudaStreamWaitEvent(cp.in, layer_done[slot], 0);   // u slot read
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(u_slot, u_host[b], bytes, cudaMemcpyHostToDevice, cp.in);
+    if (e == cudaSuccess) e = cudaEventRecord(in_done[slot], cp.in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, in_done[slot], 0);
+    if (e == cudaSuccess && b >= 2) e = cudaStreamWaitEvent(st, out_done[slot], 0);  // h slot read
+    if (e != cudaSuccess) { status = cuda_fail(e); break; }
+    status = layer_forward(s, weights, u_slot, h_slot, nullptr, ws, ws_bytes, st);
+    if (status != MOE_OK) break;
+    e = cudaEventRecord(layer_done[slot], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cp.out, layer_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h_host[b], h_slot, bytes, cudaMemcpyDeviceToHost, cp.out);
+    if (e == cudaSuccess) e = cudaEventRecord(out_done[slot], cp.out);
+    if (e != cudaSuccess) status = cuda_fail(e);
+  }
+  // the caller's stream completes only after the last copies back
+  if (status == MOE_OK) {
+    cudaError_t e = cudaStreamWaitEvent(st, out_done[(n_batches - 1) & 1], 0);
+    if (e == cudaSuccess && n_batches >= 2)
+      e = cudaStreamWaitEvent(st, out_done[n_batches & 1], 0);
+    if (e != cudaSuccess) status = cuda_fail(e);
+  }
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);  // released once they complete
+  return status;
+}
+
 // ---- moe_dispatch_static: dispatch with its scratch in a fixed array of the
 // library, for callers that cannot hand the library any device memory.
 // 2 x 131072 int32 = 1 MiB: chunk histograms and chunk bases of dispatch.

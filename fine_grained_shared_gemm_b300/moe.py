@@ -76,6 +76,9 @@ _SIGNATURES = {
     "moe_layer_forward": (ctypes.c_int, [_S, _W, _P, _P, ctypes.POINTER(moe_route_outputs),
                                          _P, ctypes.c_size_t, _P]),
     "moe_layer_forward_host": (ctypes.c_int, [_S, _W, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_layer_forward_host_stream": (ctypes.c_int, [_S, _W, ctypes.c_int, ctypes.POINTER(_P),
+                                                     ctypes.POINTER(_P), _P, _P, _P,
+                                                     ctypes.c_size_t, _P]),
     "moe_dispatch_static": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P]),
     "moe_update_select_bias": (ctypes.c_int, [_S, _P, _P, ctypes.c_float, _P, _P]),
     "moe_balance_stats_workspace_size": (ctypes.c_size_t, [_S]),
@@ -253,6 +256,22 @@ def moe_layer_forward_host(shape, weights: moe_weights, u_host, h_host, u_dev, h
         ctypes.byref(shape_struct(shape)), ctypes.byref(weights), _ptr(u_host), _ptr(h_host),
         _ptr(u_dev), _ptr(h_dev), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_forward_host_stream(shape, weights: moe_weights, u_hosts, h_hosts, u_dev, h_dev,
+                                  ws, stream=None):
+    """The layer on each of the host batches u_hosts[b] -> h_hosts[b] (each
+    [T, H], pinned), copies pipelined across batches; u_dev and h_dev hold
+    2·T·H elements each."""
+    if len(u_hosts) != len(h_hosts):
+        raise ValueError("one output buffer per input batch")
+    n = len(u_hosts)
+    ins = (_P * max(n, 1))(*[_ptr(t) for t in u_hosts])
+    outs = (_P * max(n, 1))(*[_ptr(t) for t in h_hosts])
+    _check("moe_layer_forward_host_stream", lib().moe_layer_forward_host_stream(
+        ctypes.byref(shape_struct(shape)), ctypes.byref(weights), n, ins, outs, _ptr(u_dev),
+        _ptr(h_dev), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def moe_layer_backward_workspace_size(shape) -> int:

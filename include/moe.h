@@ -18,7 +18,8 @@
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, except the
- *    two host pointers of moe_layer_forward_host.  The library allocates
+ *    host token buffers of moe_layer_forward_host and
+ *    moe_layer_forward_host_stream.  The library allocates
  *    nothing: scratch comes from the caller through `ws`/`ws_bytes`, sized by
  *    the matching *_workspace_size function, 256-byte aligned.
  *  - Layouts are dense row-major.  Weights follow the nn.Linear convention
@@ -32,7 +33,7 @@
  *    default stream) and returns without synchronising.  Arguments are
  *    checked on the host before anything is launched; a failed check
  *    launches nothing.  Errors are returned, never thrown.  The device-side
- *    calls (all but moe_layer_forward_host and moe_device_status) can be
+ *    calls (all but the two host-buffer forwards and moe_device_status) can be
  *    captured into a CUDA graph on a capturing stream once each has run
  *    outside a capture (the first call on a device sets the kernels'
  *    shared-memory limits); a replay repeats the call on the same buffers.
@@ -262,6 +263,29 @@ MOE_API moe_status moe_layer_forward_host(const moe_shape* shape,
                                           void* u_dev, void* h_dev, void* ws,
                                           size_t ws_bytes,
                                           moe_stream_t stream);
+
+/* The layer on a sequence of n_batches token batches in HOST memory, each
+ * [T, H] (shape->T tokens): u_host[b] in, h_host[b] out (host pointers,
+ * pinned for the copies to be asynchronous; arrays of n_batches pointers).
+ * Batch b + 1's copy to the device and batch b - 1's copy back overlap the
+ * layer on batch b, so a long sequence runs at the rate of the slower of the
+ * layer and the host link.  u_dev and h_dev are device buffers of two slots
+ * of [T, H] each (2·T·H elements), used alternately; ws:
+ * moe_layer_workspace_size(shape) bytes, reused batch after batch on
+ * `stream`.  The copies run on the library's two copy streams (as for
+ * moe_layer_forward_host); they wait for the work queued on `stream` before
+ * the call, and `stream` waits for the last copies back, so h_host[b] is
+ * complete once `stream` has completed.  Each h_host[b] is bitwise
+ * moe_layer_forward of u_host[b].  Returns MOE_ERR_INVALID_ARG for
+ * n_batches < 0 or a NULL pointer; n_batches = 0 or T = 0 does nothing. */
+MOE_API moe_status moe_layer_forward_host_stream(const moe_shape* shape,
+                                                 const moe_weights* weights,
+                                                 int n_batches,
+                                                 const void* const* u_host,
+                                                 void* const* h_host, void* u_dev,
+                                                 void* h_dev, void* ws,
+                                                 size_t ws_bytes,
+                                                 moe_stream_t stream);
 
 /* Weight gradients of moe_layer_backward (device pointers, fp32, written, not
  * accumulated): d_centroids [E, H]; dw1, dw3 [E, I, H]; dw2 [E, H, I]; the

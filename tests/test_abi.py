@@ -181,3 +181,29 @@ def test_bounded_wait_self_test_rejects_bad_limits():
     L = M.lib()
     assert L.moe_check_bounded_wait(0, None) == M.MOE_ERR_INVALID_ARG
     assert L.moe_check_bounded_wait(1000001, None) == M.MOE_ERR_INVALID_ARG
+
+
+def test_host_stream_rejects_bad_arguments_on_host():
+    """moe_layer_forward_host_stream checks its batch count, its host pointer
+    arrays, the device slots and the workspace before any copy or launch."""
+    s = _shape()
+    L = M.lib()
+    w = M.moe_weights(256, None, None, 256, 256, 256, 256, 256, 256)
+    need = L.moe_layer_workspace_size(ctypes.byref(s))
+    P = ctypes.c_void_p
+    two = (P * 2)(4096, 8192)
+    one_null = (P * 2)(4096, None)
+    f = L.moe_layer_forward_host_stream
+    assert f(ctypes.byref(s), ctypes.byref(w), -1, two, two, 256, 256, 256, need, None) == \
+        M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), ctypes.byref(w), 2, None, two, 256, 256, 256, need, None) == \
+        M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), ctypes.byref(w), 2, two, one_null, 256, 256, 256, need, None) == \
+        M.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(s), ctypes.byref(w), 2, two, two, 258, 256, 256, need, None) == \
+        M.MOE_ERR_INVALID_ARG     # device slots must be 16-byte aligned
+    assert f(ctypes.byref(s), ctypes.byref(w), 2, two, two, 256, 256, 256, need - 1, None) == \
+        M.MOE_ERR_WORKSPACE
+    # nothing to do: no copy, no launch
+    assert f(ctypes.byref(s), ctypes.byref(w), 0, None, None, None, None, 256, need, None) == \
+        M.MOE_OK

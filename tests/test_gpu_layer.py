@@ -118,6 +118,32 @@ def test_layer_host_buffers_match_device_path():
     assert torch.equal(h_host, h_dev_path.cpu())
 
 
+@pytest.mark.parametrize("n_batches", [1, 2, 5])
+def test_layer_host_stream_matches_device_path_batch_by_batch(n_batches):
+    """moe_layer_forward_host_stream over distinct host batches: every
+    output is bitwise the device-resident forward of its own batch, with
+    the copies of neighbouring batches overlapping its layer."""
+    shape = SMALL[2]
+    inp = W.make_inputs(shape, DEV, seed=8)
+    wt = M.weights_struct(inp)
+    gen = torch.Generator().manual_seed(9)
+    u_hosts = [torch.randn(tuple(inp.u.shape), generator=gen).to(inp.u.dtype).pin_memory()
+               for _ in range(n_batches)]
+    h_hosts = [torch.zeros_like(u).pin_memory() for u in u_hosts]
+    ws, _ = layer_buffers(shape, DEV)
+    u_dev = torch.empty((2,) + tuple(inp.u.shape), dtype=inp.u.dtype, device=DEV)
+    h_dev = torch.empty_like(u_dev)
+    M.moe_layer_forward_host_stream(shape, wt, u_hosts, h_hosts, u_dev, h_dev, ws)
+    torch.cuda.synchronize()
+    assert M.moe_device_status()[0] == M.MOE_OK
+    for b in range(n_batches):
+        u = u_hosts[b].to(DEV)
+        h = torch.empty_like(u)
+        M.moe_layer_forward(shape, wt, u, h, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(h_hosts[b], h.cpu()), b
+
+
 def test_layer_host_buffers_pipelined_chunks_match_device_path():
     # enough tokens for the host-buffer entry point to pipeline three chunks
     # (copies on their own streams overlapping the layer on earlier chunks)
