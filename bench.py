@@ -478,6 +478,12 @@ def measure_backward(args, shape, layer, flush, dev, peaks):
             "note": "recomputes routing and the gate/up pre-activations from u; "
                     "weight gradients fp32",
             "clocks": clk_b.summary(),
+            "backward_saved": {
+                "ms": round(b_ms, 4),
+                "tflops": round(flops / (b_ms / 1e3) / 1e12, 1),
+                "frac_of_bf16_peak": round(flops / (b_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                "note": "the same gradients from moe_layer_forward_train's saved tensors "
+                        "(timed within the training step below)"},
             "training_step": {
                 "forward_train_ms": round(f_ms, 4), "backward_saved_ms": round(b_ms, 4),
                 "gpu_launches": (forward_launches(s) + backward_launches(s, saved=True)) * K,
