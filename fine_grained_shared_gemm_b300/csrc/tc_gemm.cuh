@@ -68,7 +68,6 @@ constexpr int kBK = 64;            // contraction elements per k-block: one 128-
 constexpr int kKPS = 2;            // k-blocks per pipeline stage
 constexpr int kBM = 128;           // weight rows per CTA per tile (MMA M per CTA)
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma for 16-bit inputs
-constexpr int kNumThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
 // Epilogue scratch per epilogue warp: two 2 KB staging tiles for bulk
@@ -80,7 +79,25 @@ constexpr int kEpiWarpBytes = 7168;
 constexpr int kHandoffOffset = 4096;
 constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 family
 
-enum Epi : int { EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3, EPI_SWIGLU_BWD = 4 };
+// EPI_SWIGLU_BWD8 is EPI_SWIGLU_BWD with eight epilogue warps (and, for
+// their staging areas, two pipeline stages): for short contractions, where
+// the derivative epilogue rather than the operand stream sets the pace.
+enum Epi : int {
+  EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3, EPI_SWIGLU_BWD = 4,
+  EPI_SWIGLU_BWD8 = 5
+};
+
+__host__ __device__ constexpr bool is_swiglu_bwd(int epi) {
+  return epi == EPI_SWIGLU_BWD || epi == EPI_SWIGLU_BWD8;
+}
+
+// Epilogue warps of a launch: four, one per TMEM lane quarter, or eight
+// (two per quarter, taking alternate 32-row chunks).  Warp 0 loads, warp 1
+// issues the MMAs, the rest are the epilogue.
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() { return EPI == EPI_SWIGLU_BWD8 ? 8 : 4; }
+template <int EPI>
+__host__ __device__ constexpr int num_threads() { return 64 + 32 * epi_warps<EPI>(); }
 
 struct Params {
   CUtensorMap a[2];              // weight stacks (routed, shared): 3-D, or 5-D for SwiGLU
@@ -158,7 +175,7 @@ struct Params {
   int save;
   void* save_out[2];
   CUtensorMap save_map[2];
-  // EPI_SWIGLU_BWD: the accumulator is dm = dh W2 for the tile's rows (the
+  // EPI_SWIGLU_BWD / EPI_SWIGLU_BWD8: the accumulator is dm = dh W2 for the tile's rows (the
   // output row space of the groups: out_row0 = the rows' index into the
   // pre-activations a, c [rows, out_cols], read through bwd_map[0] and
   // bwd_map[1], boxes of 32 columns x 32 rows; routed rows
@@ -181,7 +198,7 @@ struct Params {
 
 constexpr int kMaxGroups = 1024;
 
-template <int BN, int PAIR>
+template <int BN, int PAIR, int EPI_WARPS = 4>
 struct Config {
   static_assert(PAIR == 1 || PAIR == 2, "a tile is shared by one or two CTAs");
   static constexpr int kBRows = BN / PAIR;              // token rows one CTA holds
@@ -189,7 +206,7 @@ struct Config {
   static constexpr int kStageBytes = kKPS * (kABytes + kBBytes);
   static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
   static constexpr int kPrefixBytes = ((kMaxGroups + 4) * 4 + 127) / 128 * 128;
-  static constexpr int kEpiBytes = 4 * kEpiWarpBytes;
+  static constexpr int kEpiBytes = EPI_WARPS * kEpiWarpBytes;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -676,7 +693,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
   tl.out_row = d.out_row0 + n * th;
   tl.out_col = (w * PAIR + rank) * kCols;
   tl.split = split;
-  if (EPI == EPI_SWIGLU_BWD) {
+  if (is_swiglu_bwd(EPI)) {
     tl.prow = d.pad + n * th;
     tl.pad_end = n == nt - 1 ? (d.count + p.pad_rows - 1) / p.pad_rows * p.pad_rows - n * th : th;
   }
@@ -716,9 +733,9 @@ __device__ __forceinline__ int sched_tile(const Params& p, int c, int P, int tot
 // ------------------------------------------------------------------ kernel
 
 template <int EPI, int BN, int PAIR>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(num_threads<EPI>(), 1)
     grouped_gemm_kernel(const __grid_constant__ Params p) {
-  using C = Config<BN, PAIR>;
+  using C = Config<BN, PAIR, epi_warps<EPI>()>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -730,8 +747,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 256u + 8u * a; };
   auto tempty_bar = [&](int a) { return bar0 + 272u + 8u * a; };
   const uint32_t done_bar = bar0 + 288u;
-  // EPI_SWIGLU_BWD: each epilogue warp's input-tile barrier
-  auto ld_bar = [&](int q) { return bar0 + 320u + 8u * q; };
+  // EPI_SWIGLU_BWD: each epilogue warp's input-tile barrier (by staging slot)
+  auto ld_bar = [&](int slot) { return bar0 + 320u + 8u * slot; };
   uint8_t* bar_area = smem + S * C::kStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 296);
   int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
@@ -749,11 +766,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4 * PAIR);  // lane 0 of each epilogue warp of each CTA
+      mbar_init(tempty_bar(a), epi_warps<EPI>() * PAIR);  // lane 0 of each epilogue warp of each CTA
     }
     mbar_init(done_bar, 1);
-    if (EPI == EPI_SWIGLU_BWD)
-      for (int q = 0; q < 4; ++q) mbar_init(ld_bar(q), 1);
+    if (is_swiglu_bwd(EPI))
+      for (int e = 0; e < epi_warps<EPI>(); ++e) mbar_init(ld_bar(e), 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -917,7 +934,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;  // the TMEM lane quarter this warp may read
-    float* buf = reinterpret_cast<float*>(epi_area + q * kEpiWarpBytes);
+    // with eight epilogue warps, the second warp of a quarter takes the odd chunks
+    const int ehalf = (warp - 2) >> 2;
+    const int eslot = q + 4 * ehalf;  // this warp's staging area and input barrier
+    constexpr int kChunkStride = 32 * (epi_warps<EPI>() / 4);
+    float* buf = reinterpret_cast<float*>(epi_area + eslot * kEpiWarpBytes);
     // SwiGLU hand-off: this warp's area and its partner's
     float* hand = reinterpret_cast<float*>(epi_area + q * kEpiWarpBytes + kHandoffOffset);
     const float* other_hand =
@@ -929,7 +950,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint32_t acc_ph[2] = {0u, 0u};
     uint32_t n_stores = 0;  // bulk stores this warp has issued (selects the staging buffer)
     // EPI_SWIGLU_BWD: the a and c tiles of one chunk land in this warp's
-    // staging area (a at [0, 2 KB), c at [2 KB, 4 KB)) on ld_bar(q); 16 rows
+    // staging area (a at [0, 2 KB), c at [2 KB, 4 KB)) on ld_bar(eslot); 16 rows
     // of the three outputs are staged at [4 KB, 7 KB) for 16-byte stores;
     // lane L holds the gate weight of row L of the next chunk
     uint16_t* ostg = reinterpret_cast<uint16_t*>(buf) + 2048;
@@ -942,9 +963,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     bool ld_pending = false, ld_failed = false;
     auto load_inputs = [&](int col, int row) {
       if (lane == 0) {
-        mbar_arrive_expect_tx(ld_bar(q), 4096u);
-        tma_load_2d_local(smem_u32(buf), &p.bwd_map[0], ld_bar(q), col, row);
-        tma_load_2d_local(smem_u32(buf) + 2048u, &p.bwd_map[1], ld_bar(q), col, row);
+        mbar_arrive_expect_tx(ld_bar(eslot), 4096u);
+        tma_load_2d_local(smem_u32(buf), &p.bwd_map[0], ld_bar(eslot), col, row);
+        tma_load_2d_local(smem_u32(buf) + 2048u, &p.bwd_map[1], ld_bar(eslot), col, row);
       }
       ld_pending = true;
     };
@@ -963,21 +984,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (t < 0) break;
       const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
       // the first chunk's inputs are on their way while the MMAs run
-      const bool bwd_active = EPI == EPI_SWIGLU_BWD && !ld_failed &&
-                              tl.out_col + q * 32 < p.out_cols && tl.n_valid > 0;
+      const int c_first = 32 * ehalf;  // this warp's first chunk
+      const bool bwd_active = is_swiglu_bwd(EPI) && !ld_failed &&
+                              tl.out_col + q * 32 < p.out_cols && c_first < tl.n_valid;
       if (bwd_active) {
         const int f0 = tl.out_col + q * 32;
-        if (lane == 0)   // every chunk's a and c boxes into L2
-          for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+        if (lane == 0)   // this warp's chunks' a and c boxes into L2
+          for (int c0 = c_first; c0 < tl.n_valid; c0 += kChunkStride) {
             tma_prefetch_2d(&p.bwd_map[0], f0, tl.out_row + c0);
             tma_prefetch_2d(&p.bwd_map[1], f0, tl.out_row + c0);
           }
-        load_inputs(f0, tl.out_row);
-        load_gate(tl, 0);
+        load_inputs(f0, tl.out_row + c_first);
+        load_gate(tl, c_first);
       }
       const bool ready = mbar_wait(tfull_bar(a0), acc_ph[a0]);
       // all four epilogue warps leave together, so no named barrier is left half-arrived
-      if (!named_bar_and(1, 128, ready)) {
+      if (!named_bar_and(1, 32 * epi_warps<EPI>(), ready)) {
         if (!ready) raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
         break;
       }
@@ -1135,7 +1157,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     q * 32);
         }
       };
-      if constexpr (EPI == EPI_SWIGLU_BWD) {
+      if constexpr (is_swiglu_bwd(EPI)) {
         // This lane's feature f0 + lane, 32 token rows per chunk: dm from
         // the accumulator, a and c from the chunk's input tiles (the next
         // chunk's are requested as soon as these are read), da / dc / g act
@@ -1143,19 +1165,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // summed over the warp's 32 features.  Chunks past the tile's valid
         // rows (its group's padding) are zeros.
         const int f0 = tl.out_col + q * 32;
-        if (bwd_active) {
+        if (cols_ok && f0 < p.out_cols) {
           const int nf = p.out_cols;
           const uint16_t* in = reinterpret_cast<const uint16_t*>(buf);
-          for (int c0 = 0; c0 < tl.pad_end; c0 += 32) {
+          for (int c0 = c_first; c0 < tl.pad_end; c0 += kChunkStride) {
             const int nrow = max(0, min(32, tl.n_valid - c0));
             const long long r0 = static_cast<long long>(tl.out_row) + c0;
             float av[32], cv[32], dm[32];
             const float g_lane = gate_next;
-            load_gate(tl, c0 + 32);  // the next chunk's, in flight during this one
+            load_gate(tl, c0 + kChunkStride);  // the next chunk's, in flight during this one
             uint32_t v[32];
             if (nrow > 0) tmem_ld32(tlane + static_cast<uint32_t>(a0 * BN + c0), v);
             if (nrow > 0 && !ld_failed) {
-              if (!mbar_wait(ld_bar(q), ld_ph)) {
+              if (!mbar_wait(ld_bar(eslot), ld_ph)) {
                 raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
                 ld_failed = true;
               } else {
@@ -1174,7 +1196,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               // proxy refills them
               fence_proxy_async_smem();
               __syncwarp();
-              if (c0 + 32 < tl.n_valid) load_inputs(f0, tl.out_row + c0 + 32);
+              if (c0 + kChunkStride < tl.n_valid) load_inputs(f0, tl.out_row + c0 + kChunkStride);
 #pragma unroll
               for (int j = 0; j < 32; ++j) dm[j] = j < nrow ? __uint_as_float(v[j]) : 0.0f;
             } else {
@@ -1239,7 +1261,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       a0 ^= 1;
     }
     // no input tile may land after the CTA exits
-    if (EPI == EPI_SWIGLU_BWD && ld_pending && !mbar_wait(ld_bar(q), ld_ph))
+    if (is_swiglu_bwd(EPI) && ld_pending && !mbar_wait(ld_bar(eslot), ld_ph))
       raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
     if (lane == 0) bulk_wait_all();  // every bulk store has completed before the CTA exits
     __syncwarp();
