@@ -627,7 +627,7 @@ def memory_kernel_bytes(s: W.MoEShape) -> dict:
 
 def run_memory_kernels(args):
     """Times the memory-bound kernels of one layer step (route, dispatch's
-    three kernels and row gather, combine) on a workload's token batch,
+    three kernels and row scatter, combine) on a workload's token batch,
     without allocating expert weights: the expert outputs combine reads are
     seeded random rows.  L2 is flushed before every timed launch."""
     dev = torch.device("cuda", 0)

@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(256) grad_combine_kernel(
       __syncwarp();
       t_loaded = t;
     }
+#pragma unroll 2
     for (int v = v0 + lane; v < v1; v += 32) {
       float acc[V], y[V];
       V16::load(dh + static_cast<size_t>(t) * H + v * V, acc);

@@ -27,6 +27,10 @@ __global__ void __launch_bounds__(256) combine_kernel(
       s_w[wib][lane] = __ldg(topk_w + static_cast<size_t>(t) * k + lane);
     }
     __syncwarp();
+    // two vectors a lane per pass: the loads of the second are issued with
+    // the first's, doubling the bytes in flight (V3-shaped batch: 291 -> 236
+    // us, 0.70 -> 0.87 of the copy rate; unrolling by 4 gained nothing)
+#pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
       float acc[V], y[V];
       Vec16<T>::load(u + static_cast<size_t>(t) * H + v * V, acc);
