@@ -722,7 +722,8 @@ def run_cuda(args):
     for n, name in enumerate(names):
         shape = W.SHAPES[name]
         entry, layer = measure_forward(args, shape, dev, flush, world, peaks, barrier)
-        if not args.no_backward and name == BACKWARD_WORKLOAD:
+        if not args.no_backward and (name == BACKWARD_WORKLOAD or
+                                     (args.backward and name == args.workload)):
             entry["backward"] = measure_backward(args, shape, layer, flush, dev, peaks)
         if n == 0 and rank == 0 and world == 1 and not args.no_cpu_baseline:
             cpu = cpu_baseline(shape, layer, args.cpu_sample)
@@ -923,6 +924,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the timed moe_layer_backward leg")
+    ap.add_argument("--backward", action="store_true",
+                    help="time moe_layer_backward on the chosen workload too (by default "
+                         "only the DeepSeekMoE-16B-shaped workload gets the backward leg)")
     ap.add_argument("--only", action="store_true",
                     help="time the chosen workload only, not the extra ones")
     ap.add_argument("--memory-kernels", action="store_true",

@@ -130,6 +130,11 @@ SHAPES = {
             description="V3-shaped prefill layer cut to 32 routed experts and 1024 "
                         "tokens: 256 rows per expert as in the full layer"),
         MoEShape(
+            name="dsmoe16b_e16_bf16", T=4096, H=2048, n_routed=16, n_shared=2,
+            top_k=6, inter=1408, gate=GATE_SOFTMAX, act=ACT_SWIGLU, dtype="bf16",
+            description="DeepSeekMoE-16B-shaped layer cut to 16 routed experts and "
+                        "4096 tokens: 1536 rows per routed expert as in the full layer"),
+        MoEShape(
             name="sweep_m16_e32_bf16", T=16384, H=2048, n_routed=32, n_shared=0,
             top_k=4, inter=256, gate=GATE_SOFTMAX, act=ACT_SWIGLU, dtype="bf16",
             description="granularity m=16 expert shape (width 256, 2048 rows per "
