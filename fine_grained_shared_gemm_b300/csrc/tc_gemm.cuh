@@ -672,7 +672,12 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int* prefix, 
     nt = prefix[lo + 1] - prefix[lo];
     local = t - prefix[lo] * nw;
   }
-  const int w = local / nt, n = local - w * nt;
+  // Token tile major within a group: the weight tiles of one token tile are
+  // consecutive.  With weight-tile-major order and an even number of
+  // clusters, a group's tiles of one token-tile position all went to the
+  // clusters of one parity: dW1/dW3's half-width last column tiles (I =
+  // 1408) left the odd clusters 17 % short of work (1100 -> 1033 us).
+  const int n = local / nw, w = local - n * nw;
   const int th = BN;  // full tiles of BN rows, then the tail
   constexpr int kCols = (EPI == EPI_SWIGLU) ? kBM / 2 : kBM;  // output columns per CTA
   Tile tl;
