@@ -568,6 +568,7 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
     layer_s = sum(step_ms) / len(step_ms) / 1e3
     offsets = layer.off.cpu().numpy()
     flops = expert_flops(shape)
+    graph_entry = None
     if is_decode(shape):
         roof = decode_roofline(shape, offsets, layer_s, ffn_s, peaks)
         roof["kernel"] = "moe_layer_forward (all 10 launches of one step)"
@@ -577,6 +578,33 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
     roof.update({"traffic": recorded_traffic(shape.name),
                  "peak_source": f"{peaks.get('_source', 'measured')} (burst)",
                  "ms_per_launch": round((layer_s if is_decode(shape) else ffn_s) * 1e3, 4)})
+    if is_decode(shape):
+        # the same step captured once into a CUDA graph and replayed, as a
+        # decode loop over fixed shapes runs it (the same ten kernels)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            layer.step()
+        for _ in range(max(1, args.warmup)):
+            g.replay()
+        barrier()
+        for i in range(K):
+            flush.zero_()
+            starts[i].record()
+            g.replay()
+            ends[i].record()
+        barrier()
+        st, code = M.moe_device_status()
+        if st != M.MOE_OK:
+            raise RuntimeError(f"device status {st} code {code} in the graph replays")
+        g_s = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K / 1e3
+        g_roof = decode_roofline(shape, offsets, g_s, ffn_s, peaks)
+        graph_entry = {"ms_per_step": round(g_s * 1e3, 4),
+                       "tokens_per_s": round(shape.T / g_s, 1),
+                       "achieved": g_roof["achieved"], "unit": g_roof["unit"],
+                       "frac": g_roof["frac"],
+                       "note": "the layer step captured into a CUDA graph and replayed"}
+        del g
     entry = {
         "value": round(value, 1), "unit": "tokens/s",
         "ms_per_step": round(total_s / K * 1e3, 4),
@@ -599,6 +627,8 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
         "gpu_launches": layer.launches_per_step * K,
         "clocks": clk.summary(),
     }
+    if graph_entry is not None:
+        entry["graph_replay"] = graph_entry
     del u_host, h_host, u_dev, u_slots, h_slots
     return entry, layer
 
