@@ -299,15 +299,15 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
     p.out_ld = I;
     p.out[0] = B.dh1p;
     p.out[1] = B.gactp;
-    // a and c in boxes of 32 columns x 32 rows (the bf16 output-map shape)
-    MOE_TRY(make_out_map(&p.bwd_map[0], B.a, static_cast<uint64_t>(Rall), I));
-    MOE_TRY(make_out_map(&p.bwd_map[1], B.c, static_cast<uint64_t>(Rall), I));
+    // a and c in boxes of 32 columns x 16 rows (half an epilogue chunk)
+    MOE_TRY(make_out_map(&p.bwd_map[0], B.a, static_cast<uint64_t>(Rall), I, 16));
+    MOE_TRY(make_out_map(&p.bwd_map[1], B.c, static_cast<uint64_t>(Rall), I, 16));
     p.bwd_gate = B.row_gate;
     p.bwd_dg = B.dg_part;
     p.bwd_routed_rows = Tk;
     p.pad_rows = kSegAlign;
-    // eight epilogue warps (two pipeline stages) when the contraction is
-    // short enough for the epilogue to set the pace
+    // eight epilogue warps when the contraction is short enough for the
+    // epilogue to set the pace
     if (H <= kBwdEpi8MaxK) MOE_TRY(launch_ffn<tc::EPI_SWIGLU_BWD8>(p, bn, st));
     else MOE_TRY(launch_ffn<tc::EPI_SWIGLU_BWD>(p, bn, st));
   } else {

@@ -14,6 +14,7 @@ enum : int {
   DEV_ERR_TIMEOUT_MMA = 2,
   DEV_ERR_TIMEOUT_EPILOGUE = 4,
   DEV_ERR_BAD_EXPERT = 8,
+  DEV_ERR_SMEM_SHORT = 16,  // launched with less dynamic shared memory than its layout
 };
 
 // Upper bound on any single wait inside a kernel (nanoseconds of the global

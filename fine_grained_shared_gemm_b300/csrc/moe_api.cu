@@ -215,7 +215,7 @@ moe_status make_token_maps(CUtensorMap* maps, const void* base, uint64_t rows, u
 // shared-memory limit and the grid are set up once per device.
 template <int EPI, int BN, int PAIR>
 cudaLaunchConfig_t tc_config(cudaLaunchAttribute* attr, cudaStream_t st) {
-  using C = tc::Config<BN, PAIR, tc::epi_warps<EPI>()>;
+  using C = tc::EpiConfig<EPI, BN, PAIR>;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -232,7 +232,7 @@ cudaLaunchConfig_t tc_config(cudaLaunchAttribute* attr, cudaStream_t st) {
 
 template <int EPI, int BN, int PAIR>
 moe_status tc_grid(int* grid) {
-  using C = tc::Config<BN, PAIR, tc::epi_warps<EPI>()>;
+  using C = tc::EpiConfig<EPI, BN, PAIR>;
   auto kern = tc::grouped_gemm_kernel<EPI, BN, PAIR>;
   static int grid_for[64] = {0};
   int dev = 0;

@@ -72,16 +72,20 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kNumBoxes = 5;       // token-tile TMA boxes of 16, 32, 64, 128, 256 rows
 // Epilogue scratch per epilogue warp: two 2 KB staging tiles for bulk
 // stores (32 x 32 bf16, or one 32 x 32 fp32 tile over both) and the SwiGLU
-// hand-off area (16 x 33 floats); or, for the SwiGLU derivative, a chunk's
-// a and c tiles (4 KB) and three 16-row output tiles (3 KB).  With 7 KB a
-// warp the 256-token pair tile still keeps three pipeline stages.
+// hand-off area (16 x 33 floats).  With 7 KB a warp the 256-token pair tile
+// still keeps three pipeline stages.
 constexpr int kEpiWarpBytes = 7168;
+// The SwiGLU-derivative epilogues keep 3.5 KB a warp: 16 rows of a chunk's a
+// and c inputs, and 8 staged rows of its three outputs.  That leaves room for
+// three pipeline stages beside eight epilogue warps.
+constexpr int kBwdInBytes = 2 * 16 * 32 * 2;     // a and c, 16 rows x 32 features
+constexpr int kBwdStageBytes = 3 * 8 * 32 * 2;   // da, dc, g act: 8 rows x 32 features
 constexpr int kHandoffOffset = 4096;
 constexpr int kSmemLimit = 232448; // dynamic shared memory per block, sm_100 family
 
-// EPI_SWIGLU_BWD8 is EPI_SWIGLU_BWD with eight epilogue warps (and, for
-// their staging areas, two pipeline stages): for short contractions, where
-// the derivative epilogue rather than the operand stream sets the pace.
+// EPI_SWIGLU_BWD8 is EPI_SWIGLU_BWD with eight epilogue warps: for short
+// contractions, where the derivative epilogue rather than the operand stream
+// sets the pace.
 enum Epi : int {
   EPI_SWIGLU = 0, EPI_RELU = 1, EPI_BF16 = 2, EPI_F32 = 3, EPI_SWIGLU_BWD = 4,
   EPI_SWIGLU_BWD8 = 5
@@ -98,6 +102,11 @@ template <int EPI>
 __host__ __device__ constexpr int epi_warps() { return EPI == EPI_SWIGLU_BWD8 ? 8 : 4; }
 template <int EPI>
 __host__ __device__ constexpr int num_threads() { return 64 + 32 * epi_warps<EPI>(); }
+// bytes of shared scratch per epilogue warp
+template <int EPI>
+__host__ __device__ constexpr int epi_warp_bytes() {
+  return is_swiglu_bwd(EPI) ? kBwdInBytes + kBwdStageBytes : kEpiWarpBytes;
+}
 
 struct Params {
   CUtensorMap a[2];              // weight stacks (routed, shared): 3-D, or 5-D for SwiGLU
@@ -198,7 +207,7 @@ struct Params {
 
 constexpr int kMaxGroups = 1024;
 
-template <int BN, int PAIR, int EPI_WARPS = 4>
+template <int BN, int PAIR, int EPI_WARPS = 4, int EPI_WARP_BYTES = kEpiWarpBytes>
 struct Config {
   static_assert(PAIR == 1 || PAIR == 2, "a tile is shared by one or two CTAs");
   static constexpr int kBRows = BN / PAIR;              // token rows one CTA holds
@@ -206,7 +215,7 @@ struct Config {
   static constexpr int kStageBytes = kKPS * (kABytes + kBBytes);
   static constexpr int kBarBytes = 512;                 // barriers, TMEM slot, descriptors
   static constexpr int kPrefixBytes = ((kMaxGroups + 4) * 4 + 127) / 128 * 128;
-  static constexpr int kEpiBytes = EPI_WARPS * kEpiWarpBytes;
+  static constexpr int kEpiBytes = EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int kFit =
       (kSmemLimit - 1024 - kBarBytes - kPrefixBytes - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -218,6 +227,11 @@ struct Config {
   static_assert(kSmemBytes <= kSmemLimit, "shared memory over the sm_100-family limit");
   static_assert(BN % kStep == 0 && kBRows <= 256, "token tile");
 };
+
+// The configuration of one epilogue mode: the kernel and the host's launch
+// (its dynamic shared memory) both take it from here.
+template <int EPI, int BN, int PAIR>
+using EpiConfig = Config<BN, PAIR, epi_warps<EPI>(), epi_warp_bytes<EPI>()>;
 
 // ------------------------------------------------------------------ PTX
 
@@ -740,7 +754,7 @@ __device__ __forceinline__ int sched_tile(const Params& p, int c, int P, int tot
 template <int EPI, int BN, int PAIR>
 __global__ void __launch_bounds__(num_threads<EPI>(), 1)
     grouped_gemm_kernel(const __grid_constant__ Params p) {
-  using C = Config<BN, PAIR, epi_warps<EPI>()>;
+  using C = EpiConfig<EPI, BN, PAIR>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -759,6 +773,17 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
   int* s_prefix = reinterpret_cast<int*>(bar_area + C::kBarBytes);
   uint8_t* epi_area = bar_area + C::kBarBytes + C::kPrefixBytes;
 
+  {
+    // the layout above must fit the launch's allocation: a launch that
+    // disagrees reports it and does nothing (every CTA of a cluster sees
+    // the same size, so none waits on a partner that has left)
+    uint32_t dyn;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (dyn < static_cast<uint32_t>(C::kSmemBytes)) {
+      if (threadIdx.x == 0) raise_device_error(DEV_ERR_SMEM_SHORT);
+      return;
+    }
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR == 2 ? cluster_rank() : 0u;
   const int first = PAIR == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
@@ -943,7 +968,7 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
     const int ehalf = (warp - 2) >> 2;
     const int eslot = q + 4 * ehalf;  // this warp's staging area and input barrier
     constexpr int kChunkStride = 32 * (epi_warps<EPI>() / 4);
-    float* buf = reinterpret_cast<float*>(epi_area + eslot * kEpiWarpBytes);
+    float* buf = reinterpret_cast<float*>(epi_area + eslot * epi_warp_bytes<EPI>());
     // SwiGLU hand-off: this warp's area and its partner's
     float* hand = reinterpret_cast<float*>(epi_area + q * kEpiWarpBytes + kHandoffOffset);
     const float* other_hand =
@@ -954,11 +979,11 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
     int a0 = 0;
     uint32_t acc_ph[2] = {0u, 0u};
     uint32_t n_stores = 0;  // bulk stores this warp has issued (selects the staging buffer)
-    // EPI_SWIGLU_BWD: the a and c tiles of one chunk land in this warp's
-    // staging area (a at [0, 2 KB), c at [2 KB, 4 KB)) on ld_bar(eslot); 16 rows
-    // of the three outputs are staged at [4 KB, 7 KB) for 16-byte stores;
+    // SwiGLU derivative: 16 rows of a chunk's a and c land in this warp's
+    // scratch (a at [0, 1 KB), c at [1 KB, 2 KB)) on ld_bar(eslot); 8 rows of
+    // the three outputs are staged at [2 KB, 3.5 KB) for 16-byte stores;
     // lane L holds the gate weight of row L of the next chunk
-    uint16_t* ostg = reinterpret_cast<uint16_t*>(buf) + 2048;
+    uint16_t* ostg = reinterpret_cast<uint16_t*>(buf) + kBwdInBytes / 2;
     float gate_next = 1.0f;
     auto load_gate = [&](const Tile& tl, int c0) {
       const long long r = static_cast<long long>(tl.out_row) + c0 + lane;
@@ -968,9 +993,10 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
     bool ld_pending = false, ld_failed = false;
     auto load_inputs = [&](int col, int row) {
       if (lane == 0) {
-        mbar_arrive_expect_tx(ld_bar(eslot), 4096u);
+        mbar_arrive_expect_tx(ld_bar(eslot), static_cast<uint32_t>(kBwdInBytes));
         tma_load_2d_local(smem_u32(buf), &p.bwd_map[0], ld_bar(eslot), col, row);
-        tma_load_2d_local(smem_u32(buf) + 2048u, &p.bwd_map[1], ld_bar(eslot), col, row);
+        tma_load_2d_local(smem_u32(buf) + kBwdInBytes / 2, &p.bwd_map[1], ld_bar(eslot), col,
+                          row);
       }
       ld_pending = true;
     };
@@ -988,17 +1014,18 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
       const int t = sched_tile(p, first, stride, total, i);
       if (t < 0) break;
       const Tile tl = decode_tile<EPI, BN, PAIR>(p, s_prefix, t, rank);
-      // the first chunk's inputs are on their way while the MMAs run
+      // the first chunk's first 16 input rows are on their way while the MMAs run
       const int c_first = 32 * ehalf;  // this warp's first chunk
       const bool bwd_active = is_swiglu_bwd(EPI) && !ld_failed &&
                               tl.out_col + q * 32 < p.out_cols && c_first < tl.n_valid;
       if (bwd_active) {
         const int f0 = tl.out_col + q * 32;
-        if (lane == 0)   // this warp's chunks' a and c boxes into L2
-          for (int c0 = c_first; c0 < tl.n_valid; c0 += kChunkStride) {
-            tma_prefetch_2d(&p.bwd_map[0], f0, tl.out_row + c0);
-            tma_prefetch_2d(&p.bwd_map[1], f0, tl.out_row + c0);
-          }
+        if (lane == 0)   // this warp's chunks' a and c boxes (16 rows each) into L2
+          for (int c0 = c_first; c0 < tl.n_valid; c0 += kChunkStride)
+            for (int r = c0; r < c0 + 32 && r < tl.n_valid; r += 16) {
+              tma_prefetch_2d(&p.bwd_map[0], f0, tl.out_row + r);
+              tma_prefetch_2d(&p.bwd_map[1], f0, tl.out_row + r);
+            }
         load_inputs(f0, tl.out_row + c_first);
         load_gate(tl, c_first);
       }
@@ -1164,11 +1191,11 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
       };
       if constexpr (is_swiglu_bwd(EPI)) {
         // This lane's feature f0 + lane, 32 token rows per chunk: dm from
-        // the accumulator, a and c from the chunk's input tiles (the next
-        // chunk's are requested as soon as these are read), da / dc / g act
-        // staged 16 rows at a time and stored as 16-byte vectors, <dm, act>
-        // summed over the warp's 32 features.  Chunks past the tile's valid
-        // rows (its group's padding) are zeros.
+        // the accumulator; a and c 16 rows at a time from the input tile (the
+        // next 16 rows are requested as soon as these are read); da / dc /
+        // g act staged 8 rows at a time and stored as 16-byte vectors;
+        // <dm, act> summed over the warp's 32 features.  Rows past the
+        // tile's valid rows (its group's padding) are zeros.
         const int f0 = tl.out_col + q * 32;
         if (cols_ok && f0 < p.out_cols) {
           const int nf = p.out_cols;
@@ -1176,71 +1203,80 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
           for (int c0 = c_first; c0 < tl.pad_end; c0 += kChunkStride) {
             const int nrow = max(0, min(32, tl.n_valid - c0));
             const long long r0 = static_cast<long long>(tl.out_row) + c0;
-            float av[32], cv[32], dm[32];
+            float dm[32];
             const float g_lane = gate_next;
             load_gate(tl, c0 + kChunkStride);  // the next chunk's, in flight during this one
             uint32_t v[32];
             if (nrow > 0) tmem_ld32(tlane + static_cast<uint32_t>(a0 * BN + c0), v);
-            if (nrow > 0 && !ld_failed) {
-              if (!mbar_wait(ld_bar(eslot), ld_ph)) {
-                raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
-                ld_failed = true;
-              } else {
-                ld_ph ^= 1u;
-                ld_pending = false;
-              }
-            }
-            if (nrow > 0 && !ld_failed) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                av[j] = j < nrow ? __bfloat162float(__ushort_as_bfloat16(in[j * 32 + lane])) : 0.0f;
-                cv[j] = j < nrow ? __bfloat162float(__ushort_as_bfloat16(in[1024 + j * 32 + lane]))
-                                 : 0.0f;
-              }
-              // every lane's reads of the tiles are ordered before the async
-              // proxy refills them
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (c0 + kChunkStride < tl.n_valid) load_inputs(f0, tl.out_row + c0 + kChunkStride);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) dm[j] = j < nrow ? __uint_as_float(v[j]) : 0.0f;
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) av[j] = cv[j] = dm[j] = 0.0f;
-            }
-            // 16 rows at a time: the three outputs into the staging tiles,
-            // then out as 16-byte vectors (4 lanes per 64-byte row segment)
+            for (int j = 0; j < 32; ++j) dm[j] = j < nrow ? __uint_as_float(v[j]) : 0.0f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-#pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                const int j = h * 16 + jj;
-                const float g = __shfl_sync(0xffffffffu, g_lane, j);
-                // sigmoid(a) = (1 + tanh(a / 2)) / 2, as in the forward's SiLU
-                const float sg = fmaf(0.5f, tanh_approx(0.5f * av[j]), 0.5f);
-                const float si = av[j] * sg;
-                const float act = si * cv[j];
-                const float gd = g * dm[j];
-                ostg[jj * 32 + lane] = __bfloat16_as_ushort(
-                    __float2bfloat16_rn(gd * cv[j] * sg * (1.0f + av[j] * (1.0f - sg))));
-                ostg[512 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(gd * si));
-                ostg[1024 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(g * act));
-                dm[j] *= act;  // this lane's share of <dm, act> for row j
+              const int hrow = nrow - 16 * h;  // valid rows among this half's 16
+              float av[16], cv[16];
+              if (hrow > 0 && !ld_failed) {
+                if (!mbar_wait(ld_bar(eslot), ld_ph)) {
+                  raise_device_error(DEV_ERR_TIMEOUT_EPILOGUE);
+                  ld_failed = true;
+                } else {
+                  ld_ph ^= 1u;
+                  ld_pending = false;
+                }
               }
-              __syncwarp();
+              if (hrow > 0 && !ld_failed) {
 #pragma unroll
-              for (int i = 0; i < 6; ++i) {
-                const int vi = i * 32 + lane;        // 16-byte vector: output, row, 8 columns
-                const int o = vi >> 6, row = (vi >> 2) & 15, c8 = (vi & 3) * 8;
-                const uint4 val = *reinterpret_cast<const uint4*>(ostg + o * 512 + row * 32 + c8);
-                // outputs 0, 1: dh1's da and dc halves (pitch 2·nf); 2: g act
-                __nv_bfloat16* const base =
-                    static_cast<__nv_bfloat16*>(o < 2 ? p.out[0] : p.out[1]) + (o == 1 ? nf : 0);
-                const size_t pitch = o < 2 ? 2 * static_cast<size_t>(nf) : static_cast<size_t>(nf);
-                *reinterpret_cast<uint4*>(
-                    base + static_cast<size_t>(tl.prow + c0 + h * 16 + row) * pitch + f0 + c8) = val;
+                for (int j = 0; j < 16; ++j) {
+                  av[j] = j < hrow ? __bfloat162float(__ushort_as_bfloat16(in[j * 32 + lane])) : 0.0f;
+                  cv[j] = j < hrow ? __bfloat162float(__ushort_as_bfloat16(in[512 + j * 32 + lane]))
+                                   : 0.0f;
+                }
+                // every lane's reads of the tile are ordered before the async
+                // proxy refills it
+                fence_proxy_async_smem();
+                __syncwarp();
+                // next: this chunk's second half, or the warp's next chunk
+                const int next = h == 0 ? c0 + 16 : c0 + kChunkStride;
+                if (next < tl.n_valid) load_inputs(f0, tl.out_row + next);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) av[j] = cv[j] = 0.0f;
               }
-              __syncwarp();  // the staging tiles are read before the next rows fill them
+              // 8 rows at a time: the three outputs into the staging tiles,
+              // then out as 16-byte vectors (4 lanes per 64-byte row segment)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const int k = e * 8 + jj;   // row within the half
+                  const int j = h * 16 + k;   // row within the chunk
+                  const float g = __shfl_sync(0xffffffffu, g_lane, j);
+                  // sigmoid(a) = (1 + tanh(a / 2)) / 2, as in the forward's SiLU
+                  const float sg = fmaf(0.5f, tanh_approx(0.5f * av[k]), 0.5f);
+                  const float si = av[k] * sg;
+                  const float act = si * cv[k];
+                  const float gd = g * dm[j];
+                  ostg[jj * 32 + lane] = __bfloat16_as_ushort(
+                      __float2bfloat16_rn(gd * cv[k] * sg * (1.0f + av[k] * (1.0f - sg))));
+                  ostg[256 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(gd * si));
+                  ostg[512 + jj * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(g * act));
+                  dm[j] *= act;  // this lane's share of <dm, act> for row j
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                  const int vi = i * 32 + lane;        // 16-byte vector: output, row, 8 columns
+                  const int o = vi >> 5, row = (vi >> 2) & 7, c8 = (vi & 3) * 8;
+                  const uint4 val = *reinterpret_cast<const uint4*>(ostg + o * 256 + row * 32 + c8);
+                  // outputs 0, 1: dh1's da and dc halves (pitch 2·nf); 2: g act
+                  __nv_bfloat16* const base =
+                      static_cast<__nv_bfloat16*>(o < 2 ? p.out[0] : p.out[1]) + (o == 1 ? nf : 0);
+                  const size_t pitch = o < 2 ? 2 * static_cast<size_t>(nf) : static_cast<size_t>(nf);
+                  *reinterpret_cast<uint4*>(
+                      base + static_cast<size_t>(tl.prow + c0 + h * 16 + e * 8 + row) * pitch + f0 +
+                      c8) = val;
+                }
+                __syncwarp();  // the staging tiles are read before the next rows fill them
+              }
             }
             // sum over the 32 lanes, scattered so that lane j ends with row j
 #pragma unroll

@@ -123,7 +123,10 @@ MOE_API const char* moe_status_string(int status);
 MOE_API int moe_last_cuda_error(void);
 
 /* Synchronises `stream`, then reads and clears this device's error word,
- * which kernels set when a bounded wait expires (no kernel traps or hangs).
+ * which kernels set instead of trapping or hanging: bit 1, 2 or 4 when a
+ * bounded wait of the grouped GEMM's producer, MMA or epilogue role
+ * expires, 8 for an expert index out of range, 16 for a grouped-GEMM launch
+ * with less dynamic shared memory than its layout (it then does nothing).
  * *code receives the raw word (0 = clean).  Returns MOE_ERR_TIMEOUT if the
  * word was set, MOE_ERR_CUDA if the synchronisation failed, else MOE_OK. */
 MOE_API moe_status moe_device_status(moe_stream_t stream, int32_t* code);
