@@ -41,6 +41,9 @@ SHAPES = [
     # group-limited routing (V3 style): 32 experts in 8 groups, 3 groups kept
     _shape("bwd_groups", T=400, n_routed=32, n_shared=1, top_k=4, inter=128,
            gate=W.GATE_SIGMOID_BIAS, bias_range=0.1, n_groups=8, topk_groups=3),
+    # H above 4096: the derivative epilogue on four warps; I = 384 leaves the
+    # second CTA of the last pair tile no features
+    _shape("bwd_wide_h_four_warps", T=90, H=4224, n_routed=6, n_shared=1, top_k=2, inter=384),
 ]
 
 
