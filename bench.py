@@ -320,11 +320,12 @@ class Layer:
         self.ws_d = M.alloc_workspace(M.moe_dispatch_workspace_size(s), dev)
         self.ws_f = M.alloc_workspace(M.moe_expert_ffn_workspace_size(s), dev)
         self.ws_l = M.alloc_workspace(M.moe_layer_workspace_size(s), dev)
-        self.launches_per_step = 10
+        self.ws_r = M.alloc_workspace(M.moe_router_logits_workspace_size(s), dev)
+        self.launches_per_step = forward_launches(s)
 
     def step(self, ev=None):
         s, i = self.s, self.inp
-        M.moe_router_logits(s, i.u, i.centroids, i.logit_offset, self.logits)
+        M.moe_router_logits(s, i.u, i.centroids, i.logit_offset, self.logits, self.ws_r)
         M.moe_route(s, self.logits, i.select_bias, self.idx, self.w)
         M.moe_dispatch(s, self.idx, i.u, self.off, self.row_token, self.slot_row, self.u_perm,
                        self.ws_d)
@@ -365,9 +366,27 @@ def backward_launches(s: W.MoEShape, saved: bool = False) -> int:
     return n
 
 
+def router_splits(s: W.MoEShape) -> int:
+    """Contraction ranges of the layer's router-logits GEMM (the library's
+    rule: bf16 batches with few 128-expert x 64-token tiles cut H so that
+    about 128 CTAs stream it, in whole two-k-block stages, at most 32)."""
+    if s.dtype != "bf16" or s.T <= 0:
+        return 1
+    cdiv = lambda a, b: -(-a // b)
+    tiles = cdiv(s.n_routed, 128) * cdiv(s.T, 64)
+    nkb = cdiv(s.H, 64)
+    want = min(32, 128 // tiles, nkb // 2)
+    if want < 2:
+        return 1
+    per = 2 * cdiv(nkb, want * 2)
+    n = cdiv(nkb, per)
+    return n if n >= 2 else 1
+
+
 def forward_launches(s: W.MoEShape) -> int:
-    """Kernel launches of one moe_layer_forward(_train) call."""
-    return 10 if s.top_k > 0 else 7
+    """Kernel launches of one moe_layer_forward(_train) call (one more, the
+    partial logits' sum, when the router GEMM is split)."""
+    return (10 if s.top_k > 0 else 7) + (1 if router_splits(s) > 1 else 0)
 
 
 def measure_backward(args, shape, layer, flush, dev, peaks):

@@ -197,15 +197,16 @@ moe_status layer_backward(const moe_shape* s, const moe_weights* wt, const void*
   // ---- the forward's routing, recomputed unless saved
   if (saved == nullptr) {
     const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
-    MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, B.logits, st));
+    MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, B.logits, nullptr, st));
     MOE_TRY(do_route(s, B.logits, bias, B.idx, B.w, nullptr, st));
     MOE_TRY(do_dispatch(s, B.idx, u, B.offsets, B.row_token, B.slot_row, B.x_perm,
                         B.dispatch_ws, st));
   }
   if (Tk > 0) {
-    const int blocks = std::max(1, std::min(cdiv(T, 8), num_sms() * 16));
-    scatter_token_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(dh), T, s->top_k, B.slot_row, H, B.d_perm);
+    const RowSplit rs = row_split(T, H / 8, 16);
+    scatter_token_rows<__nv_bfloat16><<<rs.blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(dh), T, s->top_k, B.slot_row, H, rs.nseg,
+        rs.seg_vecs, B.d_perm);
     MOE_CUDA(cudaGetLastError());
     row_gate_kernel<<<cdiv(Tk, 256), 256, 0, st>>>(B.slot_row, B.w, Tk, B.row_gate);
     MOE_CUDA(cudaGetLastError());

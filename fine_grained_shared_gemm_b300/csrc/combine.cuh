@@ -2,7 +2,10 @@
 // (page "02 · 细粒度 MoE：从 Mixtral 到 DeepSeekMoE", §3.1 Eq. 9–11: shared
 // experts, gate-weighted routed experts, residual).  fp32 accumulation in this
 // fixed order and one rounding to the output type, so the result is the same
-// on every run.  One warp per token, 16-byte vectors along H.
+// on every run.  A warp takes one (token, segment of the row) work item at a
+// time, 16-byte vectors along H: one segment per token for large batches,
+// several for small ones so that enough warps are busy (each vector's sum is
+// the same whichever warp computes it).
 #pragma once
 
 #include "common.cuh"
@@ -13,14 +16,18 @@ template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(
     const T* __restrict__ u, const T* __restrict__ y_perm, const T* __restrict__ y_shared,
     const float* __restrict__ topk_w, const int32_t* __restrict__ slot_row, int n_tokens, int H,
-    int k, int Ks, T* __restrict__ h) {
+    int k, int Ks, int nseg, int seg_vecs, T* __restrict__ h) {
   constexpr int V = Vec16<T>::N;
   __shared__ int s_row[8][32];
   __shared__ float s_w[8][32];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H / V;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += warps) {
+  const long long items = static_cast<long long>(n_tokens) * nseg;
+  for (long long it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps) {
+    const int t = static_cast<int>(it / nseg);
+    const int v0 = static_cast<int>(it - static_cast<long long>(t) * nseg) * seg_vecs;
+    const int v1 = min(nvec, v0 + seg_vecs);
     __syncwarp();
     if (lane < k) {  // k <= 32: slot s's row and weight, broadcast through shared memory
       s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
@@ -31,7 +38,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     // the first's, doubling the bytes in flight (V3-shaped batch: 291 -> 236
     // us, 0.70 -> 0.87 of the copy rate; unrolling by 4 gained nothing)
 #pragma unroll 2
-    for (int v = lane; v < nvec; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
       float acc[V], y[V];
       Vec16<T>::load(u + static_cast<size_t>(t) * H + v * V, acc);
       for (int j = 0; j < Ks; ++j) {

@@ -146,18 +146,24 @@ template <typename T>
 __global__ void __launch_bounds__(256) scatter_token_rows(const T* __restrict__ u, int T_tokens,
                                                           int k,
                                                           const int32_t* __restrict__ slot_row,
-                                                          int H, T* __restrict__ u_perm) {
+                                                          int H, int nseg, int seg_vecs,
+                                                          T* __restrict__ u_perm) {
   constexpr int kMaxK = 32;
   __shared__ int s_row[8][kMaxK];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = H * static_cast<int>(sizeof(T)) / 16;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T_tokens; t += warps) {
+  // work items (token, segment of its row), as in the combine
+  const long long items = static_cast<long long>(T_tokens) * nseg;
+  for (long long it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += warps) {
+    const int t = static_cast<int>(it / nseg);
+    const int v0 = static_cast<int>(it - static_cast<long long>(t) * nseg) * seg_vecs;
+    const int v1 = min(nvec, v0 + seg_vecs);
     __syncwarp();
     if (lane < k) s_row[wib][lane] = __ldg(slot_row + static_cast<size_t>(t) * k + lane);
     __syncwarp();
     const uint4* src = reinterpret_cast<const uint4*>(u + static_cast<size_t>(t) * H);
-    for (int v = lane; v < nvec; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
       const uint4 x = __ldg(src + v);
       for (int j = 0; j < k; ++j) {
         const int r = s_row[wib][j];

@@ -353,8 +353,38 @@ FfnWs carve_ffn(void* ws, const moe_shape* s) {
   return w;
 }
 
+// Router logits of a batch with few (128-expert x 64-token) tiles: the
+// contraction over H is cut into ranges of whole pipeline stages so that
+// about kRouterCtas CTAs stream it, each range's partial logits written apart
+// and added in order after (decode: 3 tiles over H = 7168 take 28 ranges of
+// four k-blocks).  Large batches have enough tiles and stay whole.  Fixed
+// constants, not the device's SM count, so the workspace size is the same
+// on every device.
+constexpr int kRouterCtas = 128;
+constexpr int kRouterMaxSplits = 32;
+int router_splits(const moe_shape* s, int* blocks_per_range) {
+  *blocks_per_range = 0;
+  if (s->dtype != MOE_DTYPE_BF16 || s->T <= 0) return 1;
+  const int tiles = cdiv(s->n_routed, tc::kBM) * cdiv(s->T, 64);
+  const int nkb = cdiv(s->H, tc::kBK);
+  const int want = std::min({kRouterMaxSplits, kRouterCtas / tiles, nkb / tc::kKPS});
+  if (want < 2) return 1;
+  const int per = tc::kKPS * cdiv(nkb, want * tc::kKPS);
+  const int S = cdiv(nkb, per);
+  if (S < 2) return 1;
+  *blocks_per_range = per;
+  return S;
+}
+
+size_t router_ws_bytes(const moe_shape* s) {
+  int per = 0;
+  const int S = router_splits(s, &per);
+  return S > 1 ? static_cast<size_t>(S) * s->T * s->n_routed * 4 : 0;
+}
+
 struct LayerWs {
   float* logits;
+  float* logit_part;  // the router's partial logits [S, T, E] (nullptr: not split)
   int32_t* idx;
   float* w;
   int32_t* offsets;
@@ -380,6 +410,8 @@ LayerWs carve_layer(void* ws, const moe_shape* s) {
   };
   LayerWs L;
   L.logits = static_cast<float*>(take(T * E * 4));
+  const size_t part_bytes = router_ws_bytes(s);
+  L.logit_part = part_bytes ? static_cast<float*>(take(part_bytes)) : nullptr;
   L.idx = static_cast<int32_t*>(take(T * k * 4));
   L.w = static_cast<float*>(take(T * k * 4));
   L.offsets = static_cast<int32_t*>(take((E + 1) * 4));
@@ -398,6 +430,28 @@ LayerWs carve_layer(void* ws, const moe_shape* s) {
 
 int route_blocks(int T) { return std::max(1, std::min(cdiv(T, 8), num_sms() * 8)); }
 
+// Row work of the scatter and the combine: a warp takes one (token, segment)
+// item at a time.  A batch of fewer tokens than about 32 warps per SM gets
+// several segments per token row, each of whole 32-vector passes (decode:
+// 64 tokens of 896 vectors become 64 x 28 items); larger batches keep one
+// segment per token.  `blocks` covers the items with 8-warp blocks, at most
+// `max_blocks_per_sm` a SM (a grid-stride loop takes the rest).
+struct RowSplit {
+  int nseg, seg_vecs, blocks;
+};
+RowSplit row_split(int T, int nvec, int max_blocks_per_sm) {
+  RowSplit r{1, nvec, 1};
+  const int per = T > 0 ? num_sms() * 32 / T : 1;
+  if (per > 1 && nvec > 32) {
+    r.seg_vecs = 32 * cdiv(nvec, 32 * per);
+    r.nseg = cdiv(nvec, r.seg_vecs);
+  }
+  const long long items = static_cast<long long>(T) * r.nseg;
+  r.blocks = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(cdiv(items, 8LL), static_cast<long long>(num_sms()) * max_blocks_per_sm)));
+  return r;
+}
+
 // Blocks of `threads` that are resident on the device at once (one wave) for
 // a kernel without dynamic shared memory; cached per kernel and device.
 template <typename K>
@@ -415,8 +469,10 @@ int one_wave_blocks(K kernel, int threads) {
   return cached[dev];
 }
 
+// part: scratch for the router_splits ranges' partial logits, or nullptr to
+// run the contraction whole.
 moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
-                            const float* off, float* logits, cudaStream_t st) {
+                            const float* off, float* logits, float* part, cudaStream_t st) {
   const int T = s->T, E = s->n_routed, H = s->H;
   if (T == 0) return MOE_OK;
   if (s->dtype == MOE_DTYPE_F32) {
@@ -452,6 +508,22 @@ moe_status do_router_logits(const moe_shape* s, const void* u, const void* cent,
   p.col_offset = off;
   const int bn = (T > 64 && p.n_wtiles * cdiv(T, 256) >= num_sms()) ? 256 : 64;
   const int tiles = p.n_wtiles * cdiv(T, bn);
+  int per = 0;
+  const int S = part != nullptr && bn == 64 ? router_splits(s, &per) : 1;
+  if (S > 1) {
+    // the ranges' partial logits, without the offset; then their sum
+    p.k_splits = S;
+    p.k_split_blocks = per;
+    p.split_stride = static_cast<long long>(T) * E;
+    p.out[0] = p.out[1] = part;
+    p.col_offset = nullptr;
+    MOE_TRY((launch_tc<tc::EPI_F32, 64, 1>(p, tiles * S, st)));
+    const long long n = static_cast<long long>(T) * E;
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, num_sms() * 4LL));
+    sum_logit_partials_kernel<<<blocks, 256, 0, st>>>(part, S, n, E, off, logits);
+    MOE_CUDA(cudaGetLastError());
+    return MOE_OK;
+  }
   return bn == 256 ? launch_tc<tc::EPI_F32, 256, 1>(p, tiles, st)
                    : launch_tc<tc::EPI_F32, 64, 1>(p, tiles, st);
 }
@@ -494,14 +566,15 @@ moe_status do_dispatch(const moe_shape* s, const int32_t* idx, const void* u, in
   dispatch_scatter<<<n_chunks, kDispatchWarps * 32, kDispatchWarps * E * 4, st>>>(
       idx, T, k, E, d.chunk_base, row_token, slot_row);
   MOE_CUDA(cudaGetLastError());
-  const int blocks = std::max(1, std::min(cdiv(T, 8), num_sms() * 16));
+  const int esize = s->dtype == MOE_DTYPE_F32 ? 4 : 2;
+  const RowSplit rs = row_split(T, s->H * esize / 16, 16);
   if (s->dtype == MOE_DTYPE_F32)
-    scatter_token_rows<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(u), T, k,
-                                                      slot_row, s->H,
-                                                      static_cast<float*>(u_perm));
+    scatter_token_rows<float><<<rs.blocks, 256, 0, st>>>(static_cast<const float*>(u), T, k,
+                                                         slot_row, s->H, rs.nseg, rs.seg_vecs,
+                                                         static_cast<float*>(u_perm));
   else
-    scatter_token_rows<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(u), T, k, slot_row, s->H,
+    scatter_token_rows<__nv_bfloat16><<<rs.blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(u), T, k, slot_row, s->H, rs.nseg, rs.seg_vecs,
         static_cast<__nv_bfloat16*>(u_perm));
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
@@ -649,17 +722,17 @@ moe_status do_combine(const moe_shape* s, const void* u, const void* y_perm,
   const int T = s->T;
   if (T == 0) return MOE_OK;
   const bool f32 = s->dtype == MOE_DTYPE_F32;
-  const int blocks = route_blocks(T);
+  const RowSplit rs = row_split(T, s->H / (f32 ? 4 : 8), 8);
   if (f32)
-    combine_kernel<float><<<blocks, 256, 0, st>>>(
+    combine_kernel<float><<<rs.blocks, 256, 0, st>>>(
         static_cast<const float*>(u), static_cast<const float*>(y_perm),
         static_cast<const float*>(y_shared), w, slot_row, T, s->H, s->top_k, s->n_shared,
-        static_cast<float*>(h));
+        rs.nseg, rs.seg_vecs, static_cast<float*>(h));
   else
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+    combine_kernel<__nv_bfloat16><<<rs.blocks, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(u), static_cast<const __nv_bfloat16*>(y_perm),
         static_cast<const __nv_bfloat16*>(y_shared), w, slot_row, T, s->H, s->top_k,
-        s->n_shared, static_cast<__nv_bfloat16*>(h));
+        s->n_shared, rs.nseg, rs.seg_vecs, static_cast<__nv_bfloat16*>(h));
   MOE_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -787,7 +860,7 @@ moe_status layer_forward(const moe_shape* s, const moe_weights* wt, const void* 
     save_c = S.c;
   }
   const float* bias = s->gate == MOE_GATE_SIGMOID_BIAS ? wt->select_bias : nullptr;
-  MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, logits, st));
+  MOE_TRY(do_router_logits(s, u, wt->centroids, wt->logit_offset, logits, L.logit_part, st));
   MOE_TRY(do_route(s, logits, bias, idx, w, nullptr, st));
   MOE_TRY(do_dispatch(s, idx, u, offsets, row_token, slot_row, u_perm, L.dispatch_ws, st));
   MOE_TRY(do_expert_ffn(s, wt, u, u_perm, offsets, L.y_perm, L.y_shared, L.ffn_ws, st, save_a,
@@ -850,13 +923,20 @@ MOE_API size_t moe_layer_workspace_size(const moe_shape* s) {
   return check_shape(s) == MOE_OK ? carve_layer(nullptr, s).total : 0;
 }
 
+MOE_API size_t moe_router_logits_workspace_size(const moe_shape* s) {
+  return check_shape(s) == MOE_OK ? router_ws_bytes(s) : 0;
+}
+
 MOE_API moe_status moe_router_logits(const moe_shape* s, const void* u, const void* centroids,
-                                     const float* logit_offset, float* logits,
-                                     moe_stream_t stream) {
+                                     const float* logit_offset, float* logits, void* ws,
+                                     size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_shape(s));
   if (!ok_ptr(centroids) || !ok_opt(logit_offset)) return MOE_ERR_INVALID_ARG;
   if (s->T > 0 && (!ok_ptr(u) || !ok_ptr(logits))) return MOE_ERR_INVALID_ARG;
-  return do_router_logits(s, u, centroids, logit_offset, logits, cs(stream));
+  const size_t need = router_ws_bytes(s);
+  if (ws != nullptr && (!al16(ws) || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  float* part = ws != nullptr && need > 0 ? static_cast<float*>(ws) : nullptr;
+  return do_router_logits(s, u, centroids, logit_offset, logits, part, cs(stream));
 }
 
 MOE_API moe_status moe_route(const moe_shape* s, const float* logits, const float* select_bias,

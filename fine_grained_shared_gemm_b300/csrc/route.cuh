@@ -62,6 +62,20 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
+// Router logits cut along H into S contraction ranges (few-token batches):
+// logits[t, e] = (part[0][t, e] + ... + part[S-1][t, e]) + o_e, the ranges
+// added in order so that the result is the same on every run.
+__global__ void __launch_bounds__(256) sum_logit_partials_kernel(
+    const float* __restrict__ part, int S, long long n, int E, const float* __restrict__ offset,
+    float* __restrict__ logits) {
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
+    float acc = __ldg(part + i);
+    for (int sp = 1; sp < S; ++sp) acc += __ldg(part + static_cast<long long>(sp) * n + i);
+    if (offset != nullptr) acc += __ldg(offset + i % E);
+    logits[i] = acc;
+  }
+}
+
 // NPL logits per lane: expert e = lane + 32 * i.  Requires E <= 32 * NPL and
 // top_k <= 32.
 template <int NPL>

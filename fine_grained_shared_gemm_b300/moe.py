@@ -68,7 +68,8 @@ _SIGNATURES = {
     "moe_dispatch_workspace_size": (ctypes.c_size_t, [_S]),
     "moe_expert_ffn_workspace_size": (ctypes.c_size_t, [_S]),
     "moe_layer_workspace_size": (ctypes.c_size_t, [_S]),
-    "moe_router_logits": (ctypes.c_int, [_S, _P, _P, _P, _P, _P]),
+    "moe_router_logits_workspace_size": (ctypes.c_size_t, [_S]),
+    "moe_router_logits": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_route": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (ctypes.c_int, [_S, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_S, _W, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -169,6 +170,10 @@ def moe_layer_workspace_size(shape) -> int:
     return lib().moe_layer_workspace_size(ctypes.byref(shape_struct(shape)))
 
 
+def moe_router_logits_workspace_size(shape) -> int:
+    return lib().moe_router_logits_workspace_size(ctypes.byref(shape_struct(shape)))
+
+
 def moe_balance_stats_workspace_size(shape) -> int:
     return lib().moe_balance_stats_workspace_size(ctypes.byref(shape_struct(shape)))
 
@@ -180,10 +185,11 @@ def moe_device_status(stream=None):
     return st, code.value
 
 
-def moe_router_logits(shape, u, centroids, logit_offset, logits, stream=None):
+def moe_router_logits(shape, u, centroids, logit_offset, logits, ws=None, stream=None):
     _check("moe_router_logits", lib().moe_router_logits(
         ctypes.byref(shape_struct(shape)), _ptr(u), _ptr(centroids), _ptr(logit_offset),
-        _ptr(logits), _stream(stream)))
+        _ptr(logits), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def moe_route(shape, logits, select_bias, topk_idx, topk_w, kth_gap=None, stream=None):

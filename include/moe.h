@@ -144,14 +144,22 @@ MOE_API moe_status moe_check_bounded_wait(uint32_t limit_us, moe_stream_t stream
 MOE_API size_t moe_dispatch_workspace_size(const moe_shape* shape);
 MOE_API size_t moe_expert_ffn_workspace_size(const moe_shape* shape);
 MOE_API size_t moe_layer_workspace_size(const moe_shape* shape);
+MOE_API size_t moe_router_logits_workspace_size(const moe_shape* shape);
 
 /* Router logits z[t, i] = u_tᵀ e_i (+ logit_offset[i]), fp32 accumulation
  * (page "02 · 细粒度 MoE", §2.1 Eq. 8: the score is a function of u_tᵀ e_i).
- * u [T, H], centroids [E, H] in shape->dtype; logits [T, E] fp32 out. */
+ * u [T, H], centroids [E, H] in shape->dtype; logits [T, E] fp32 out.
+ * ws: NULL, or moe_router_logits_workspace_size(shape) bytes (16-byte
+ * aligned; fewer give MOE_ERR_WORKSPACE).  With it, a bf16 batch with few
+ * 128-expert x 64-token tiles (decode-sized) has its contraction over H cut
+ * into ranges whose partial logits land in ws and are added in range order,
+ * then the offset; without it (or when the size is 0) the contraction runs
+ * whole.  Each way gives the same logits on every run; the two differ only
+ * by fp32 rounding. */
 MOE_API moe_status moe_router_logits(const moe_shape* shape, const void* u,
                                      const void* centroids,
-                                     const float* logit_offset, float* logits,
-                                     moe_stream_t stream);
+                                     const float* logit_offset, float* logits, void* ws,
+                                     size_t ws_bytes, moe_stream_t stream);
 
 /* Scores, top-k choice and gate weights per token from fp32 logits
  * (§2.1 Eq. 6–8 for softmax; §3.1 Eq. 12–15 and ch. 7 §7.4 for sigmoid+bias).

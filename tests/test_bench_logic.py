@@ -92,6 +92,33 @@ def test_backward_launch_counts():
     assert bench.forward_launches(s) == 10 and bench.forward_launches(relu) == 7
 
 
+def test_router_split_rule():
+    # decode: 3 tiles of 128 experts x 64 tokens over 112 k-blocks -> 28
+    # ranges of 4 k-blocks, and one more launch (the partial sums)
+    dec = W.SHAPES["decode_bf16"]
+    assert bench.router_splits(dec) == 28
+    assert bench.forward_launches(dec) == 11
+    # prefill batches have enough tiles to stay whole
+    for name in ("v3_prefill_bf16", "dsmoe16b_bf16"):
+        assert bench.router_splits(W.SHAPES[name]) == 1
+        assert bench.forward_launches(W.SHAPES[name]) == 10
+    # H = 128: one stage of two k-blocks, nothing to cut; fp32 runs unsplit
+    tiny = W.MoEShape("t", T=8, H=128, n_routed=8, n_shared=0, top_k=2, inter=64)
+    assert bench.router_splits(tiny) == 1
+    f32 = W.MoEShape("f", T=8, H=1024, n_routed=8, n_shared=0, top_k=2, inter=64, dtype="f32")
+    assert bench.router_splits(f32) == 1
+    # the library's own rule: its workspace holds exactly the ranges' partials
+    from fine_grained_shared_gemm_b300 import moe as M
+    for s in (dec, W.SHAPES["decode_e48_bf16"], W.SHAPES["v3_prefill_bf16"], tiny, f32):
+        n = bench.router_splits(s)
+        assert M.moe_router_logits_workspace_size(s) == (n * s.T * s.n_routed * 4 if n > 1 else 0)
+    # at most 32 ranges of at least one two-k-block stage each
+    for H in (256, 384, 1024, 2048, 7168):
+        s = W.MoEShape("h", T=16, H=H, n_routed=64, n_shared=0, top_k=2, inter=64)
+        n = bench.router_splits(s)
+        assert 2 <= n <= min(32, H // 128)
+
+
 def test_traffic_record_needs_the_current_kernel_source():
     assert bench.recorded_traffic("no_such_workload") is None
     rec = bench.recorded_traffic("dsmoe16b_bf16")

@@ -126,15 +126,42 @@ def test_route_zero_tokens_and_zero_k():
 ], ids=lambda s: s.name)
 def test_router_logits(shape):
     inp = W.make_inputs(shape, DEV, seed=3)
-    logits = torch.empty((shape.T, shape.n_routed), dtype=torch.float32, device=DEV)
-    M.moe_router_logits(shape, inp.u, inp.centroids, inp.logit_offset, logits)
     u, e = np64(inp.u), np64(inp.centroids)
     off = None if inp.logit_offset is None else np64(inp.logit_offset)
     ref = O.router_logits(u, e, off).astype(np.float64)
-    got = logits.cpu().numpy().astype(np.float64)
     # fp32 accumulation of H products: bounded by a small multiple of Σ|u_d e_d|
     bound = 1e-5 * (np.abs(u) @ np.abs(e).T) + 1e-6
-    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) - bound))
+    # the contraction whole (no workspace), and with the workspace, which cuts
+    # it into ranges for few-tile batches (the decode shape: 28 ranges)
+    need = M.moe_router_logits_workspace_size(shape)
+    if shape.name == "lg_bf16_decode":
+        assert need == 28 * shape.T * shape.n_routed * 4
+    outs = []
+    for ws in (None, M.alloc_workspace(need, DEV)):
+        logits = torch.full((shape.T, shape.n_routed), float("nan"), dtype=torch.float32,
+                            device=DEV)
+        M.moe_router_logits(shape, inp.u, inp.centroids, inp.logit_offset, logits, ws)
+        got = logits.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) - bound))
+        outs.append(got)
+        if ws is not None:   # the ranges are added in a fixed order: the same on every run
+            M.moe_router_logits(shape, inp.u, inp.centroids, inp.logit_offset, logits, ws)
+            assert np.array_equal(logits.cpu().numpy().astype(np.float64), got)
+    if need == 0:
+        assert np.array_equal(outs[0], outs[1])
+
+
+def test_router_logits_rejects_a_short_workspace():
+    shape = S("lg_short_ws", T=64, H=1024, n_routed=64)
+    need = M.moe_router_logits_workspace_size(shape)
+    assert need > 0
+    inp = W.make_inputs(shape, DEV, seed=3)
+    logits = torch.empty((shape.T, shape.n_routed), dtype=torch.float32, device=DEV)
+    st = M.lib().moe_router_logits(M.ctypes.byref(M.shape_struct(shape)), M._ptr(inp.u),
+                                   M._ptr(inp.centroids), None, M._ptr(logits),
+                                   M._ptr(M.alloc_workspace(need, DEV)), need - 16, None)
+    assert st == M.MOE_ERR_WORKSPACE
+    assert M.moe_device_status() == (M.MOE_OK, 0)
 
 
 # ---------------------------------------------------------------- dispatch
