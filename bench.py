@@ -590,7 +590,7 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
     graph_entry = None
     if is_decode(shape):
         roof = decode_roofline(shape, offsets, layer_s, ffn_s, peaks)
-        roof["kernel"] = "moe_layer_forward (all 10 launches of one step)"
+        roof["kernel"] = f"moe_layer_forward (all {layer.launches_per_step} launches of one step)"
     else:
         roof = prefill_roofline(shape, offsets, ffn_s, peaks)
         roof["kernel"] = "moe_expert_ffn (gate/up and down grouped GEMMs)"
