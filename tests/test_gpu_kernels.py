@@ -202,6 +202,23 @@ def test_dispatch_bit_exact(T, E, k, kind):
         assert (ref["counts"] == 0).any() or E <= 8   # some experts receive no token
 
 
+@pytest.mark.parametrize("T,E,k,H", [
+    (1000, 64, 6, 2176),   # 272 vectors a row in segments of 96, 96, 80
+    (64, 384, 8, 7168),    # decode-sized: 28 segments of 32 vectors a row
+    (3000, 32, 4, 1024),   # one segment a row (enough tokens)
+])
+def test_dispatch_row_segments(T, E, k, H):
+    # the row scatter splits each token row across several warps for small
+    # batches; every copy must still land whole
+    shape = S("disp_seg", T=T, H=H, n_routed=E, top_k=k)
+    idx = _idx_for(shape, seed=T + H)
+    u = torch.randn((T, H), device=DEV).to(torch.bfloat16)
+    off, row_token, slot_row, u_perm = _gpu_dispatch(shape, idx, u)
+    ref = O.dispatch(idx, E)
+    assert np.array_equal(row_token.cpu().numpy(), ref["row_token"])
+    assert torch.equal(u_perm, u[row_token.long()])
+
+
 def test_dispatch_all_tokens_to_same_experts():
     T, E, k = 777, 32, 4
     shape = S("hot", T=T, n_routed=E, top_k=k)
@@ -289,7 +306,11 @@ def test_expert_ffn(shape):
 # ---------------------------------------------------------------- combine
 
 @pytest.mark.parametrize("dtype,T,H,k,Ks", [("bf16", 333, 512, 6, 2), ("f32", 100, 256, 3, 1),
-                                           ("bf16", 50, 7168, 8, 1), ("bf16", 64, 256, 0, 2)])
+                                           ("bf16", 50, 7168, 8, 1), ("bf16", 64, 256, 0, 2),
+                                           # rows split across warps with a short last
+                                           # segment (96, 96, 80 vectors), bf16 and fp32
+                                           ("bf16", 1000, 2176, 6, 1), ("f32", 1000, 1088, 4, 1),
+                                           ("bf16", 64, 7168, 8, 1)])
 def test_combine(dtype, T, H, k, Ks):
     E = max(k, 4)
     shape = S("comb", T=T, H=H, n_routed=E, top_k=k, n_shared=Ks, dtype=dtype)
