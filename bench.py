@@ -614,7 +614,7 @@ def measure_forward(args, shape, dev, flush, world, peaks, barrier):
                  "ms_per_launch": round((layer_s if is_decode(shape) else ffn_s) * 1e3, 4)})
     if is_decode(shape):
         # the same step captured once into a CUDA graph and replayed, as a
-        # decode loop over fixed shapes runs it (the same ten kernels)
+        # decode loop over fixed shapes runs it (the same kernels)
         g = torch.cuda.CUDAGraph()
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
